@@ -1,0 +1,364 @@
+#!/usr/bin/env python3
+"""Benchmark of MLA tree-verify attention on GB300 (one JSON line on stdout).
+
+A step is one verify-attention call (partial kernel + split-K combine) over the
+4-request short-context workload (prefix 5,760, 16-node trees, 65,536-slot
+pool) unless --workload says otherwise.  Timing: CUDA events on the launching
+stream around each call, L2 flushed (256 MiB write) between calls outside the
+events, W untimed warm-up calls, K timed calls bracketed by barrier +
+synchronize.  ``value`` is microseconds per call for the whole job.
+
+--impl reference times the CPU oracle (the only other implementation of this
+path) on the host cores on a bounded row sample of the same workload and
+extrapolates to microseconds per call.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_mla_speculative_tree_gb300 import binding  # noqa: E402
+from paged_mla_speculative_tree_gb300 import workloads as W  # noqa: E402
+
+METRIC = "verify-attn µs/call, effective HBM GB/s, % of roofline (1×GB300)"
+UNIT = "us/call"
+DEFAULT_WORKLOAD = "batch4"
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "source": "fallback"}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(smax)), "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def make_workload(name):
+    if name not in W.WORKLOADS:
+        raise SystemExit(f"unknown workload {name}; choose from {sorted(W.WORKLOADS)}")
+    return W.WORKLOADS[name]()
+
+
+def device_inputs(wl, dev):
+    return dict(q=wl.q.to(dev), kv_pool=wl.kv_pool.to(dev), kv_indices=wl.kv_indices.to(dev),
+                kv_indptr=wl.kv_indptr.to(dev), out_cache_loc=wl.out_cache_loc.to(dev),
+                qo_indptr=wl.qo_indptr.to(dev), custom_mask=wl.custom_mask.to(dev),
+                mask_indptr=wl.mask_indptr.to(dev))
+
+
+STEP_INPUTS = ("q", "kv_indices", "kv_indptr", "out_cache_loc", "qo_indptr", "custom_mask", "mask_indptr")
+
+
+def cpu_oracle_timing(wl, target_s=15.0, seed=0):
+    """Times the oracle on a bounded row sample; returns (us per full call, cores, sample text)."""
+    import oracle
+    cores = oracle.default_threads()
+    H = wl.num_heads
+    total_rows = wl.total_q * H
+    rng = np.random.default_rng(seed)
+    # calibrate on a handful of rows, then size the sample for ~target_s
+    n = min(total_rows, max(cores, 16))
+    rows = np.sort(rng.choice(total_rows, size=n, replace=False))
+    t0 = time.perf_counter()
+    oracle.mla_tree_verify(wl, rows=rows, num_threads=cores)
+    dt = time.perf_counter() - t0
+    per_row = dt / n
+    n2 = int(min(total_rows, max(n, target_s / max(per_row, 1e-9))))
+    if n2 > n:
+        rows = np.sort(rng.choice(total_rows, size=n2, replace=False))
+        t0 = time.perf_counter()
+        oracle.mla_tree_verify(wl, rows=rows, num_threads=cores)
+        dt = time.perf_counter() - t0
+        n = n2
+    us_per_call = dt / n * total_rows * 1e6
+    return us_per_call, cores, f"{n} of {total_rows} (token, head) rows, seeded uniform; {dt:.1f} s"
+
+
+def run_reference(args):
+    ws, rank, local = dist_env()
+    if rank != 0:
+        return 0
+    wl = make_workload(args.workload)
+    import oracle
+    cores = oracle.default_threads()
+    H = wl.num_heads
+    total_rows = wl.total_q * H
+    rng = np.random.default_rng(123)
+    # size each step's sample so the whole run stays within a few minutes
+    probe = np.sort(rng.choice(total_rows, size=min(total_rows, max(cores, 16)), replace=False))
+    t0 = time.perf_counter()
+    oracle.mla_tree_verify(wl, rows=probe, num_threads=cores)
+    per_row = (time.perf_counter() - t0) / probe.size
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    n = int(min(total_rows, max(probe.size, budget / max(per_row, 1e-9))))
+    for _ in range(args.warmup):
+        oracle.mla_tree_verify(wl, rows=np.sort(rng.choice(total_rows, size=n, replace=False)), num_threads=cores)
+    times = []
+    for _ in range(args.steps):
+        rows = np.sort(rng.choice(total_rows, size=n, replace=False))
+        t0 = time.perf_counter()
+        oracle.mla_tree_verify(wl, rows=rows, num_threads=cores)
+        times.append((time.perf_counter() - t0) / n * total_rows * 1e6)
+    value = float(np.mean(times))
+    sample = f"{n} of {total_rows} (token, head) rows per step, seeded uniform, extrapolated to the full call"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": value / 1e3, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl.name, "bs": wl.bs, "prefix": wl.prefix_lens[0] if wl.bs else 0,
+                       "tree": wl.tree_sizes[0] if wl.bs else 0},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = make_workload(args.workload)
+    d = device_inputs(wl, dev)
+    flags = binding.FLAG_SIMT_FLOOR if args.simt else 0
+    m = binding.MlaTreeVerify(wl.bs, wl.max_q_per_req, wl.total_q, wl.max_prefix, device=local,
+                              mask_layout=wl.mask_layout, flags=flags, nsplit=args.nsplit)
+    out = torch.empty((wl.total_q, 64, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.total_q, 64), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def call():
+        m(d["q"], d["kv_pool"], d["kv_indices"], d["kv_indptr"], d["out_cache_loc"], d["qo_indptr"],
+          d["custom_mask"], d["mask_indptr"], wl.scale, out, lse)
+
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call()
+    torch.cuda.synchronize()
+    assert m.device_error() == 0, "device error word set during warm-up"
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(k & 0xff)
+            starts[k].record(stream)
+            call()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+        if ws > 1:
+            torch.distributed.barrier()
+        wall = time.perf_counter() - t_wall
+    per_call_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    ms = float(np.mean(per_call_ms))
+    if ws > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    clocks = clk.summary()
+    launches_per_call = 1 + (1 if m.plan.nsplit > 1 else 0)
+
+    # end to end through the public API with host buffers (pinned), copies inside the timed region
+    host = {k: wl_tensor(wl, k).pin_memory() for k in STEP_INPUTS}
+    out_h = torch.empty_like(out, device="cpu").pin_memory()
+    lse_h = torch.empty_like(lse, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    for _ in range(max(1, args.warmup)):
+        e2e_step(host, d, call, out, lse, out_h, lse_h)
+    torch.cuda.synchronize()
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.fill_(k & 0xff)
+        e_s[k].record(stream)
+        e2e_step(host, d, call, out, lse, out_h, lse_h)
+        e_e[k].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)]))
+
+    if rank != 0:
+        if ws > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    peaks = load_peaks()
+    flops = wl.algorithmic_flops()
+    nbytes = wl.algorithmic_bytes()
+    achieved_tf = flops / (ms * 1e-3) / 1e12
+    achieved_gbs = nbytes / (ms * 1e-3) / 1e9
+    peak_tf = peaks["bf16_tflops"]
+    roof_ms = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peak_tf * 1e12)) * 1e3
+    bound = "tensor" if flops / (peak_tf * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    traffic = load_traffic(wl.name, m.plan)
+    if bound == "tensor":
+        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                "frac": achieved_tf / peak_tf, "traffic": traffic}
+    else:
+        roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic}
+    roof.update({"peak_source": peaks["source"] + (" burst" if bound == "tensor" else ""),
+                 "timed": "whole call (partial + combine), CUDA events on the launch stream",
+                 "roofline_us": roof_ms * 1e3, "frac_of_roofline": roof_ms / ms,
+                 "effective_hbm_gbs": achieved_gbs})
+    line = {
+        "metric": METRIC, "value": ms * 1e3 / ws, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "bs": wl.bs, "prefix": wl.prefix_lens, "tree": wl.tree_sizes,
+                   "num_slots": wl.num_slots, "heads": 64, "d_qk": 576, "d_v": 512,
+                   "kernel": "simt-floor" if args.simt else "tcgen05", "nsplit": int(m.plan.nsplit),
+                   "split_keys": int(m.plan.split_keys), "parallelism": f"replicas x{ws}",
+                   "l2": "flushed between calls (256 MiB write outside the timed events)"},
+        "effective_hbm_gbs": achieved_gbs, "achieved_tflops": achieved_tf,
+        "roofline": roof, "clocks": clocks, "gpu_launches": launches_per_call * args.steps,
+        "e2e": {"value": e2e_ms * 1e3 / ws, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "wall_s_timed_region": wall,
+    }
+    if not args.no_cpu_baseline:
+        us, cores, sample = cpu_oracle_timing(wl, target_s=args.cpu_seconds)
+        line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def wl_tensor(wl, k):
+    return getattr(wl, k).contiguous()
+
+
+def e2e_step(host, d, call, out, lse, out_h, lse_h):
+    for k, t in host.items():
+        d[k].copy_(t, non_blocking=True)
+    call()
+    out_h.copy_(out, non_blocking=True)
+    lse_h.copy_(lse, non_blocking=True)
+
+
+def load_traffic(workload_name, plan):
+    """DRAM bytes per call from the committed ncu summary, if it matches this build."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    try:
+        d = json.load(open(path))
+        e = d.get(workload_name)
+        if e and e.get("kernel_rev") == kernel_revision():
+            return e.get("dram_bytes_per_call")
+    except Exception:
+        return None
+    return None
+
+
+def kernel_revision():
+    import hashlib
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "paged_mla_speculative_tree_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
+    ap.add_argument("--nsplit", type=int, default=0)
+    ap.add_argument("--simt", action="store_true", help="time the SIMT correctness-floor kernel")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,189 @@
+"""ctypes binding of the C ABI in ``include/mla_tree_verify.h``.
+
+Argument marshalling only: every step of the verify attention runs in the CUDA
+library.  There is no fallback -- if the library is missing this raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+MTV_OK = 0
+MASK_FULL_ROW = 0
+MASK_TREE_ONLY = 1
+FLAG_SIMT_FLOOR = 0x1
+DEVERR_SLOT_RANGE = 0x1
+DEVERR_INDPTR = 0x2
+DEVERR_TIMEOUT = 0x4
+PLAN_MAGIC = 0x4D545650
+ABI_VERSION = 1
+
+
+class MtvPlan(ctypes.Structure):
+    _fields_ = [
+        ("magic", ctypes.c_uint32), ("version", ctypes.c_uint32),
+        ("device", ctypes.c_int32), ("num_sms", ctypes.c_int32),
+        ("cc_major", ctypes.c_int32), ("cc_minor", ctypes.c_int32),
+        ("bs", ctypes.c_int32), ("max_q_per_req", ctypes.c_int32), ("num_heads", ctypes.c_int32),
+        ("d_latent", ctypes.c_int32), ("d_rope", ctypes.c_int32), ("mask_layout", ctypes.c_int32),
+        ("flags", ctypes.c_int32), ("row_tile", ctypes.c_int32), ("key_tile", ctypes.c_int32),
+        ("nsplit", ctypes.c_int32), ("grid_rows", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("total_q_max", ctypes.c_int64), ("max_prefix", ctypes.c_int64),
+        ("split_keys", ctypes.c_int64), ("ws_bytes", ctypes.c_uint64),
+        ("ws_part_o", ctypes.c_uint64), ("ws_part_lse", ctypes.c_uint64),
+        ("reserved", ctypes.c_int64 * 6),
+    ]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_ if not f.startswith("reserved")}
+
+
+class MtvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {strerror(code)} (code {code})")
+        self.code = code
+
+
+_lib = None
+SYMBOLS = ("mla_tree_verify_plan", "mla_tree_verify_run", "mla_tree_verify_strerror",
+           "mla_tree_verify_clear_device_error", "mla_tree_verify_read_device_error")
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(path: str | None = None):
+    """Loads the CUDA library (building it first if sources are newer)."""
+    global _lib
+    if _lib is not None and path is None:
+        return _lib
+    path = path or library_path()
+    if not os.path.exists(path):
+        raise RuntimeError(f"CUDA library not built: {path} (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    P, I32, I64, U64 = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_uint64
+    lib.mla_tree_verify_plan.argtypes = [I32, I32, I32, I64, I64, I32, I32, I32, I32, I32, I32,
+                                         ctypes.POINTER(MtvPlan), ctypes.POINTER(U64)]
+    lib.mla_tree_verify_plan.restype = I32
+    lib.mla_tree_verify_run.argtypes = [ctypes.POINTER(MtvPlan), P, P, I64, P, P, P, P, P, P,
+                                        ctypes.c_float, P, P, P, U64, P]
+    lib.mla_tree_verify_run.restype = I32
+    lib.mla_tree_verify_strerror.argtypes = [I32]
+    lib.mla_tree_verify_strerror.restype = ctypes.c_char_p
+    lib.mla_tree_verify_clear_device_error.argtypes = [P, P]
+    lib.mla_tree_verify_clear_device_error.restype = I32
+    lib.mla_tree_verify_read_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
+    lib.mla_tree_verify_read_device_error.restype = I32
+    if path == library_path():
+        _lib = lib
+    return lib
+
+
+def strerror(code: int) -> str:
+    return load().mla_tree_verify_strerror(int(code)).decode()
+
+
+def plan(device: int, bs: int, max_q_per_req: int, total_q_max: int, max_prefix: int,
+         mask_layout: int = MASK_FULL_ROW, flags: int = 0, nsplit: int = 0,
+         num_heads: int = 64, d_latent: int = 512, d_rope: int = 64) -> MtvPlan:
+    p = MtvPlan()
+    ws = ctypes.c_uint64(0)
+    rc = load().mla_tree_verify_plan(int(device), int(bs), int(max_q_per_req), int(total_q_max),
+                                      int(max_prefix), int(num_heads), int(d_latent), int(d_rope),
+                                      int(mask_layout), int(flags), int(nsplit), ctypes.byref(p),
+                                      ctypes.byref(ws))
+    if rc != MTV_OK:
+        raise MtvError(rc, "mla_tree_verify_plan")
+    return p
+
+
+def _ptr(t, dtype, name, empty=None):
+    """Device address of a tensor.  An empty tensor maps to ``empty`` (a valid
+    device address that is never dereferenced because its size is zero)."""
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor):
+        return int(t)  # raw device address
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    return t.data_ptr() if t.numel() else empty
+
+
+def _stream_handle(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def run(p: MtvPlan, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr, custom_mask,
+        mask_indptr, scale: float, out, lse, workspace, stream=None, check: bool = True) -> int:
+    """Enqueues one verify-attention pass; returns the ABI code (raises if check)."""
+    num_slots = kv_pool.shape[0] if isinstance(kv_pool, torch.Tensor) else 0
+    ws_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else 0
+    wsp = _ptr(workspace, torch.uint8, "workspace")
+    rc = load().mla_tree_verify_run(
+        ctypes.byref(p), _ptr(q, torch.bfloat16, "q", wsp), _ptr(kv_pool, torch.bfloat16, "kv_pool", wsp),
+        int(num_slots), _ptr(kv_indices, torch.int64, "kv_indices", wsp),
+        _ptr(kv_indptr, torch.int32, "kv_indptr"), _ptr(out_cache_loc, torch.int64, "out_cache_loc", wsp),
+        _ptr(qo_indptr, torch.int64, "qo_indptr"), _ptr(custom_mask, torch.uint8, "custom_mask", wsp),
+        _ptr(mask_indptr, torch.int64, "mask_indptr"), float(scale),
+        _ptr(out, torch.bfloat16, "out", wsp), _ptr(lse, torch.float32, "lse", wsp),
+        wsp, int(ws_bytes), _stream_handle(stream))
+    if check and rc != MTV_OK:
+        raise MtvError(rc, "mla_tree_verify_run")
+    return rc
+
+
+def clear_device_error(workspace, stream=None):
+    rc = load().mla_tree_verify_clear_device_error(_ptr(workspace, torch.uint8, "workspace"),
+                                                   _stream_handle(stream))
+    if rc != MTV_OK:
+        raise MtvError(rc, "mla_tree_verify_clear_device_error")
+
+
+def read_device_error(workspace, stream=None) -> int:
+    v = ctypes.c_uint32(0)
+    rc = load().mla_tree_verify_read_device_error(_ptr(workspace, torch.uint8, "workspace"),
+                                                  ctypes.byref(v), _stream_handle(stream))
+    if rc != MTV_OK:
+        raise MtvError(rc, "mla_tree_verify_read_device_error")
+    return int(v.value)
+
+
+class MlaTreeVerify:
+    """Owns a plan and a torch-allocated workspace for fixed upper bounds.
+
+    ``__call__`` takes device tensors (the SGLang-style buffers) and writes
+    ``out``/``lse``; it never synchronises, so it can be captured in a graph."""
+
+    def __init__(self, bs, max_q_per_req, total_q_max, max_prefix, device=0,
+                 mask_layout=MASK_FULL_ROW, flags=0, nsplit=0):
+        self.plan = plan(device, bs, max_q_per_req, total_q_max, max_prefix, mask_layout, flags, nsplit)
+        self.device = torch.device("cuda", device)
+        self.workspace = torch.empty(max(int(self.plan.ws_bytes), 256), dtype=torch.uint8, device=self.device)
+        clear_device_error(self.workspace)
+
+    def __call__(self, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr, custom_mask,
+                 mask_indptr, scale, out=None, lse=None, stream=None):
+        T = self.plan.total_q_max
+        if out is None:
+            out = torch.empty((T, 64, 512), dtype=torch.bfloat16, device=self.device)
+        if lse is None:
+            lse = torch.empty((T, 64), dtype=torch.float32, device=self.device)
+        run(self.plan, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr, custom_mask,
+            mask_indptr, scale, out, lse, self.workspace, stream)
+        return out, lse
+
+    def device_error(self, stream=None) -> int:
+        return read_device_error(self.workspace, stream)

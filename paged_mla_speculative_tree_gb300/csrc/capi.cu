@@ -1,0 +1,226 @@
+// C-ABI shim of the MLA tree-verify library: plan (host only, from upper
+// bounds) and run (argument checks + kernel launches on the caller's stream;
+// no sync, no allocation, capture-safe).  The split into a small extern "C"
+// surface over device pointers and a stream follows "The Glue That Makes
+// Kernels Run" -- "The Decision Architecture" (C-ABI as the integration
+// boundary) and "The Final Solder Joint" -- "Why the C-ABI Edit Matters".
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "mtv_internal.cuh"
+
+using namespace mtv;
+
+namespace {
+
+constexpr uint64_t kWsHeader = 256;
+
+uint64_t align256(uint64_t x) { return (x + 255) & ~uint64_t(255); }
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// Split-K choice for the SIMT floor: enough CTAs for ~2 waves, >= 256 keys per split.
+int choose_nsplit_simt(int num_sms, int64_t ctas_per_split, int64_t max_keys) {
+  if (ctas_per_split <= 0) return 1;
+  int64_t want = ceil_div(2 * int64_t(num_sms), ctas_per_split);
+  int64_t cap = std::max<int64_t>(1, ceil_div(max_keys, 256));
+  return int(std::max<int64_t>(1, std::min<int64_t>({want, cap, 64})));
+}
+
+}  // namespace
+
+// Defined in partial_tc.cu: picks split count for the tensor-core kernel.
+namespace mtv {
+int choose_nsplit_tc(int num_sms, int64_t pairs_per_split, int64_t max_keys, int64_t rows_total);
+extern const int kTcRowTile;
+extern const int kTcKeyTile;
+}  // namespace mtv
+
+extern "C" {
+
+const char* mla_tree_verify_strerror(int code) {
+  switch (code) {
+    case MTV_OK: return "ok";
+    case MTV_E_NULL_POINTER: return "a required pointer is NULL";
+    case MTV_E_UNSUPPORTED: return "unsupported shape (needs 64 heads, 512 latent + 64 rope dims)";
+    case MTV_E_BAD_ARGUMENT: return "bad argument (negative size, unknown mask layout or flag)";
+    case MTV_E_WORKSPACE_SMALL: return "workspace smaller than plan->ws_bytes";
+    case MTV_E_WORKSPACE_ALIGN: return "workspace not 256-byte aligned";
+    case MTV_E_BAD_PLAN: return "plan was not produced by mla_tree_verify_plan (or wrong ABI version)";
+    case MTV_E_CUDA: return "CUDA runtime call or kernel launch failed";
+    case MTV_E_DEVICE: return "device unusable (needs an sm_103 GPU; plan device must be current)";
+    default: return "unknown error code";
+  }
+}
+
+int mla_tree_verify_plan(int device, int bs, int max_q_per_req, int64_t total_q_max,
+                         int64_t max_prefix, int num_heads, int d_latent, int d_rope,
+                         int mask_layout, int flags, int nsplit_override, mtv_plan_t* plan_out,
+                         uint64_t* ws_bytes_out) {
+  if (!plan_out) return MTV_E_NULL_POINTER;
+  if (num_heads != kHeads || d_latent != kDLat || d_rope != kDRope) return MTV_E_UNSUPPORTED;
+  if (bs < 0 || max_q_per_req < 0 || total_q_max < 0 || max_prefix < 0 || nsplit_override < 0)
+    return MTV_E_BAD_ARGUMENT;
+  if (mask_layout != MTV_MASK_FULL_ROW && mask_layout != MTV_MASK_TREE_ONLY) return MTV_E_BAD_ARGUMENT;
+  if (flags & ~MTV_FLAG_SIMT_FLOOR) return MTV_E_BAD_ARGUMENT;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
+    cudaGetLastError();
+    return MTV_E_DEVICE;
+  }
+  int sms = 0, ccmaj = 0, ccmin = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ccmaj, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+      cudaDeviceGetAttribute(&ccmin, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess) {
+    cudaGetLastError();
+    return MTV_E_CUDA;
+  }
+  if (ccmaj != 10 || ccmin != 3) return MTV_E_DEVICE;
+
+  mtv_plan_t p;
+  memset(&p, 0, sizeof p);
+  p.magic = MTV_PLAN_MAGIC;
+  p.version = MTV_ABI_VERSION;
+  p.device = device;
+  p.num_sms = sms;
+  p.cc_major = ccmaj;
+  p.cc_minor = ccmin;
+  p.bs = bs;
+  p.max_q_per_req = max_q_per_req;
+  p.num_heads = num_heads;
+  p.d_latent = d_latent;
+  p.d_rope = d_rope;
+  p.mask_layout = mask_layout;
+  p.flags = flags;
+  p.total_q_max = total_q_max;
+  p.max_prefix = max_prefix;
+  const int64_t max_keys = std::max<int64_t>(1, max_prefix + max_q_per_req);
+
+  int prev = 0;
+  if (cudaGetDevice(&prev) != cudaSuccess) return MTV_E_CUDA;
+  if (prev != device && cudaSetDevice(device) != cudaSuccess) return MTV_E_CUDA;
+  cudaError_t prep;
+  if (flags & MTV_FLAG_SIMT_FLOOR) {
+    p.row_tile = kHeads;
+    p.key_tile = kSimtKeyTile;
+    p.grid_rows = max_q_per_req;
+    const int64_t ctas = int64_t(bs) * max_q_per_req;
+    p.nsplit = nsplit_override ? nsplit_override : choose_nsplit_simt(sms, ctas, max_keys);
+    prep = prepare_partial_simt();
+  } else {
+    p.row_tile = kTcRowTile;
+    p.key_tile = kTcKeyTile;
+    p.grid_rows = int(ceil_div(int64_t(max_q_per_req) * kHeads, kTcRowTile));
+    const int64_t pairs = int64_t(bs) * p.grid_rows;
+    p.nsplit = nsplit_override ? nsplit_override
+                               : choose_nsplit_tc(sms, pairs, max_keys, int64_t(bs) * max_q_per_req * kHeads);
+    prep = prepare_partial_tc();
+  }
+  if (prev != device) cudaSetDevice(prev);
+  if (prep != cudaSuccess) {
+    cudaGetLastError();
+    return MTV_E_CUDA;
+  }
+  p.nsplit = std::max(1, std::min(p.nsplit, 1024));
+  p.split_keys = ceil_div(ceil_div(max_keys, p.nsplit), p.key_tile) * p.key_tile;
+  p.nsplit = int(std::max<int64_t>(1, ceil_div(max_keys, p.split_keys)));
+
+  uint64_t ws = kWsHeader;
+  if (p.nsplit > 1) {
+    const uint64_t rows = uint64_t(total_q_max) * kHeads;
+    p.ws_part_o = ws;
+    ws = align256(ws + uint64_t(p.nsplit) * rows * kDLat * sizeof(float));
+    p.ws_part_lse = ws;
+    ws = align256(ws + uint64_t(p.nsplit) * rows * sizeof(float));
+  }
+  p.ws_bytes = ws;
+  *plan_out = p;
+  if (ws_bytes_out) *ws_bytes_out = ws;
+  return MTV_OK;
+}
+
+int mla_tree_verify_run(const mtv_plan_t* plan, const void* q, const void* kv_pool,
+                        int64_t num_slots, const int64_t* kv_indices, const int32_t* kv_indptr,
+                        const int64_t* out_cache_loc, const int64_t* qo_indptr,
+                        const uint8_t* custom_mask, const int64_t* mask_indptr, float scale,
+                        void* out, float* lse, void* workspace, uint64_t workspace_bytes,
+                        void* stream) {
+  if (!plan) return MTV_E_NULL_POINTER;
+  if (plan->magic != MTV_PLAN_MAGIC || plan->version != MTV_ABI_VERSION) return MTV_E_BAD_PLAN;
+  if (!workspace || !kv_indptr || !qo_indptr || !mask_indptr) return MTV_E_NULL_POINTER;
+  if (plan->bs > 0 && plan->total_q_max > 0 &&
+      (!q || !kv_pool || !kv_indices || !out_cache_loc || !custom_mask || !out || !lse))
+    return MTV_E_NULL_POINTER;
+  if (num_slots < 0) return MTV_E_BAD_ARGUMENT;
+  if (reinterpret_cast<uintptr_t>(workspace) & 255) return MTV_E_WORKSPACE_ALIGN;
+  if (workspace_bytes < plan->ws_bytes) return MTV_E_WORKSPACE_SMALL;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) {
+    cudaGetLastError();
+    return MTV_E_CUDA;
+  }
+  if (cur != plan->device) return MTV_E_DEVICE;
+  if (plan->bs == 0 || plan->total_q_max == 0 || plan->max_q_per_req == 0) return MTV_OK;
+
+  Params P;
+  memset(&P, 0, sizeof P);
+  P.q = static_cast<const __nv_bfloat16*>(q);
+  P.kv_pool = static_cast<const __nv_bfloat16*>(kv_pool);
+  P.num_slots = num_slots;
+  P.kv_indices = kv_indices;
+  P.kv_indptr = kv_indptr;
+  P.out_cache_loc = out_cache_loc;
+  P.qo_indptr = qo_indptr;
+  P.custom_mask = custom_mask;
+  P.mask_indptr = mask_indptr;
+  P.scale = scale;
+  P.scale_log2 = scale * kLog2e;
+  P.out = static_cast<__nv_bfloat16*>(out);
+  P.lse = lse;
+  unsigned char* ws = static_cast<unsigned char*>(workspace);
+  P.err = reinterpret_cast<unsigned*>(ws);
+  P.part_o = plan->nsplit > 1 ? reinterpret_cast<float*>(ws + plan->ws_part_o) : nullptr;
+  P.part_lse = plan->nsplit > 1 ? reinterpret_cast<float*>(ws + plan->ws_part_lse) : nullptr;
+  P.bs = plan->bs;
+  P.max_q = plan->max_q_per_req;
+  P.mask_layout = plan->mask_layout;
+  P.nsplit = plan->nsplit;
+  P.grid_rows = plan->grid_rows;
+  P.key_tile = plan->key_tile;
+  P.total_q_max = plan->total_q_max;
+  P.max_prefix = plan->max_prefix;
+  P.split_keys = plan->split_keys;
+
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = (plan->flags & MTV_FLAG_SIMT_FLOOR) ? launch_partial_simt(P, st)
+                                                      : launch_partial_tc(P, st);
+  if (e == cudaSuccess && plan->nsplit > 1) e = launch_combine(P, st);
+  if (e != cudaSuccess) return MTV_E_CUDA;
+  return MTV_OK;
+}
+
+int mla_tree_verify_clear_device_error(void* workspace, void* stream) {
+  if (!workspace) return MTV_E_NULL_POINTER;
+  if (cudaMemsetAsync(workspace, 0, sizeof(unsigned), static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+    cudaGetLastError();
+    return MTV_E_CUDA;
+  }
+  return MTV_OK;
+}
+
+int mla_tree_verify_read_device_error(const void* workspace, uint32_t* flags_out, void* stream) {
+  if (!workspace || !flags_out) return MTV_E_NULL_POINTER;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned v = 0;
+  if (cudaMemcpyAsync(&v, workspace, sizeof v, cudaMemcpyDeviceToHost, st) != cudaSuccess ||
+      cudaStreamSynchronize(st) != cudaSuccess) {
+    cudaGetLastError();
+    return MTV_E_CUDA;
+  }
+  *flags_out = v;
+  return MTV_OK;
+}
+
+}  // extern "C"

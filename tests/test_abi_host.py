@@ -1,0 +1,107 @@
+"""Host-side checks of the C ABI (no GPU needed): the library builds, loads and
+exports every declared symbol; the plan struct layout matches the header; host
+argument checks return the documented codes without touching a device."""
+import ctypes
+import os
+import re
+import subprocess
+import tempfile
+
+import pytest
+
+from paged_mla_speculative_tree_gb300 import binding, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "mla_tree_verify.h")
+
+
+def declared_functions():
+    names = []
+    for h in sorted(os.listdir(os.path.join(ROOT, "include"))):
+        if h.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", h)).read()
+            txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(mla_tree_verify\w*)\s*\(", txt, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return binding.load()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    names = declared_functions()
+    assert len(names) >= 5
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(binding.SYMBOLS) <= set(names)
+
+
+def test_plan_struct_layout_matches_header():
+    prog = r'''
+#include <stdio.h>
+#include <stddef.h>
+#include "mla_tree_verify.h"
+int main(void) {
+  printf("%zu %zu %zu %zu %zu\n", sizeof(mtv_plan_t), offsetof(mtv_plan_t, total_q_max),
+         offsetof(mtv_plan_t, split_keys), offsetof(mtv_plan_t, ws_part_lse), offsetof(mtv_plan_t, reserved));
+  return 0;
+}'''
+    with tempfile.TemporaryDirectory() as d:
+        src = os.path.join(d, "l.c")
+        exe = os.path.join(d, "l")
+        open(src, "w").write(prog)
+        subprocess.check_call(["gcc", "-I", os.path.join(ROOT, "include"), src, "-o", exe])
+        vals = list(map(int, subprocess.check_output([exe]).split()))
+    P = binding.MtvPlan
+    assert vals == [ctypes.sizeof(P), P.total_q_max.offset, P.split_keys.offset,
+                    P.ws_part_lse.offset, P.reserved.offset]
+
+
+def test_strerror_covers_codes(lib):
+    for code in range(0, -9, -1):
+        assert binding.strerror(code) != "unknown error code"
+    assert binding.strerror(-99) == "unknown error code"
+
+
+def _plan_rc(lib, **kw):
+    a = dict(device=0, bs=1, max_q=8, total_q=8, max_prefix=256, H=64, dl=512, dr=64, layout=0, flags=0,
+             nsplit=0)
+    a.update(kw)
+    p = binding.MtvPlan()
+    ws = ctypes.c_uint64()
+    return lib.mla_tree_verify_plan(a["device"], a["bs"], a["max_q"], a["total_q"], a["max_prefix"], a["H"],
+                                    a["dl"], a["dr"], a["layout"], a["flags"], a["nsplit"], ctypes.byref(p),
+                                    ctypes.byref(ws))
+
+
+def test_plan_rejects_bad_arguments_before_touching_a_device(lib):
+    assert _plan_rc(lib, H=32) == -2
+    assert _plan_rc(lib, dl=256) == -2
+    assert _plan_rc(lib, dr=0) == -2
+    assert _plan_rc(lib, layout=7) == -3
+    assert _plan_rc(lib, bs=-1) == -3
+    assert _plan_rc(lib, flags=0x10) == -3
+    assert lib.mla_tree_verify_plan(0, 1, 8, 8, 256, 64, 512, 64, 0, 0, 0, None, None) == -1
+
+
+def test_run_host_checks(lib):
+    P = binding.MtvPlan()
+    fake = ctypes.c_void_p(0x100000)  # never dereferenced: checks fail first
+    args = [fake, fake, 4096, fake, fake, fake, fake, fake, fake, 1.0, fake, fake]
+    # not a plan
+    assert lib.mla_tree_verify_run(ctypes.byref(P), *args, fake, 1 << 20, None) == -6
+    assert lib.mla_tree_verify_run(None, *args, fake, 1 << 20, None) == -1
+    P.magic, P.version, P.bs, P.total_q_max, P.max_q_per_req, P.ws_bytes = \
+        binding.PLAN_MAGIC, binding.ABI_VERSION, 1, 8, 8, 4096
+    assert lib.mla_tree_verify_run(ctypes.byref(P), *args, ctypes.c_void_p(0x100010), 1 << 20, None) == -5
+    assert lib.mla_tree_verify_run(ctypes.byref(P), *args, fake, 1024, None) == -4
+    assert lib.mla_tree_verify_run(ctypes.byref(P), *args, None, 1 << 20, None) == -1
+    nulls = list(args)
+    nulls[0] = None  # q
+    assert lib.mla_tree_verify_run(ctypes.byref(P), *nulls, fake, 1 << 20, None) == -1
+    assert lib.mla_tree_verify_clear_device_error(None, None) == -1
+    v = ctypes.c_uint32()
+    assert lib.mla_tree_verify_read_device_error(None, ctypes.byref(v), None) == -1

@@ -1,0 +1,124 @@
+"""GPU parity: the CUDA library (through the C ABI) against the CPU oracle on
+the same seeded inputs.  Small cases are compared on every row; the named
+full-size workloads on a seeded row sample (plus properties at any size)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_mla_speculative_tree_gb300 import binding
+from paged_mla_speculative_tree_gb300 import workloads as W
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+KERNELS = {"tc": 0, "simt": binding.FLAG_SIMT_FLOOR}
+
+
+@pytest.fixture(params=sorted(KERNELS))
+def flags(request):
+    return KERNELS[request.param]
+
+
+# ------------------------------------------------------------ small, every row
+
+def test_tiny_every_row(flags):
+    wl = W.tiny()
+    out, lse = G.run_gpu(wl, flags)
+    G.compare(wl, out, lse, tag="tiny")
+
+
+@pytest.mark.parametrize("nsplit", [1, 2, 3, 7])
+def test_ragged_batch_every_row(flags, nsplit):
+    g = torch.Generator().manual_seed(77)
+    parents = [W.random_parents(n, g) for n in (1, 5, 13, 3)]
+    wl = W.custom([0, 77, 300, 129], parents, 2048, seed=78)
+    out, lse = G.run_gpu(wl, flags, nsplit=nsplit)
+    G.compare(wl, out, lse, tag=f"ragged nsplit={nsplit}")
+
+
+def test_tree_only_layout(flags):
+    g = torch.Generator().manual_seed(5)
+    parents = [W.random_parents(n, g) for n in (9, 4)]
+    wl = W.custom([200, 65], parents, 1024, seed=6, mask_layout=W.MASK_TREE_ONLY)
+    out, lse = G.run_gpu(wl, flags, nsplit=2)
+    G.compare(wl, out, lse, tag="tree-only")
+
+
+def test_shapes_chain_star_and_tile_edges(flags):
+    # prefix lengths on both sides of tile boundaries, odd tree sizes
+    parents = [W.chain_parents(3), W.star_parents(64), W.chain_parents(2), W.random_parents(
+        33, torch.Generator().manual_seed(1))]
+    wl = W.custom([63, 64, 65, 127], parents, 4096, seed=9)
+    out, lse = G.run_gpu(wl, flags, nsplit=3)
+    G.compare(wl, out, lse, tag="edges")
+
+
+def test_empty_request_and_rows_without_keys(flags):
+    # request 1 has no tree tokens; request 2 has no prefix and an all-zero mask
+    parents = [W.random_parents(4, torch.Generator().manual_seed(2)), [], [W.ROOT, 0, 1]]
+    wl = W.custom([40, 10, 0], parents, 512, seed=4)
+    mip = wl.mask_indptr.numpy()
+    wl.custom_mask[mip[2]:mip[3]] = 0
+    out, lse = G.run_gpu(wl, flags, nsplit=2)
+    G.compare(wl, out, lse, tag="empty")
+    H = 64
+    assert np.all(np.isneginf(lse[4 * H:7 * H])) and np.all(out[4 * H:7 * H] == 0)
+
+
+def test_prefix_mask_columns_ignored(flags):
+    wl = W.custom([100], [W.random_parents(6, torch.Generator().manual_seed(3))], 512, seed=8)
+    base_o, base_l = G.run_gpu(wl, flags)
+    wl.custom_mask.view(6, 106)[:, :100] = 0
+    o2, l2 = G.run_gpu(wl, flags)
+    assert np.array_equal(base_o, o2) and np.array_equal(base_l, l2)
+
+
+def test_rows_past_total_q_untouched(flags):
+    wl = W.custom([50], [W.chain_parents(4)], 256, seed=12)
+    out, lse = G.run_gpu(wl, flags, total_q_max=9)
+    H = 64
+    assert np.all(np.isnan(out[4 * H:])) and np.all(np.isnan(lse[4 * H:]))
+    G.compare(wl, out[:4 * H], lse[:4 * H], tag="capacity")
+
+
+def test_bad_slot_sets_error_and_is_masked(flags):
+    wl = W.custom([70], [W.chain_parents(5)], 512, seed=14)
+    bad = wl.kv_indices.clone()
+    bad[33] = 10_000_000  # beyond the pool
+    d = G.to_device(wl)
+    d["kv_indices"] = bad.cuda()
+    out, lse, err, _ = G.run_gpu(wl, flags, dev_tensors=d, return_err=True)
+    assert err & binding.DEVERR_SLOT_RANGE
+    # the offending key is treated as masked: compare with the oracle without it
+    keep = torch.cat([wl.kv_indices[:33], wl.kv_indices[34:]])
+    wl2 = W.custom([69], [W.chain_parents(5)], 512, seed=14)
+    ref = oracle.mla_tree_verify(wl, kv_indices=keep, kv_indptr=torch.tensor([0, 69], dtype=torch.int32),
+                                 custom_mask=wl2.custom_mask, mask_indptr=wl2.mask_indptr)
+    G.compare(wl, out, lse, ref=ref, tag="bad slot")
+
+
+def test_request_beyond_plan_bounds_is_flagged(flags):
+    wl = W.custom([300], [W.chain_parents(4)], 1024, seed=15)
+    out, lse, err, _ = G.run_gpu(wl, flags, max_prefix=200, return_err=True)
+    assert err & binding.DEVERR_INDPTR
+
+
+# ------------------------------------------------------------ named workloads (sampled)
+
+@pytest.mark.parametrize("name", ["batch4", "long_contig", "long_random", "mixed"])
+def test_named_workload_sampled(flags, name):
+    wl = W.WORKLOADS[name]()
+    out, lse = G.run_gpu(wl, flags)
+    rows = G.sample_rows(wl, 96, seed=hash(name) % 1000)
+    G.compare(wl, out, lse, rows=rows, tag=name)
+    assert np.all(np.isfinite(lse)) and np.all(np.isfinite(out))
+
+
+def test_long_contiguous_equals_random_slots(flags):
+    a, b = W.long_context(True), W.long_context(False)
+    oa, la = G.run_gpu(a, flags)
+    ob, lb = G.run_gpu(b, flags)
+    assert np.array_equal(oa, ob) and np.array_equal(la, lb)
