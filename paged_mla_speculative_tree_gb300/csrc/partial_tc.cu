@@ -1,26 +1,530 @@
-// Tensor-core (tcgen05/TMEM) split-K partial kernel -- under construction.
+// Tensor-core (tcgen05 / TMEM) split-K partial kernel for MLA tree-verify
+// attention on sm_103a.
+//
+// Work unit: a pair of CTAs (a 2-CTA cluster) owns 128 query rows of one
+// request -- two draft-tree tokens x 64 heads -- and one split of the
+// request's keys (prefix keys through kv_indices, then the tree tokens through
+// out_cache_loc: "The Final Solder Joint" -- "The Three-Edits Sequence").
+// Each latent row gathered from the paged pool is shared by all 64 heads x
+// both tokens of the tile ("The Glue That Connects" -- "The Context": the
+// MLA latent is read once instead of once per head).
+//
+// The 576 contraction dims are split between the two CTAs: CTA c holds latent
+// dims [256c, 256c+256) and rope dims [32c, 32c+32).  Per 64-key tile:
+//   1. producers gather the CTA's 576 bytes of each latent row with cp.async
+//      into a 128B-swizzled K-major tile (64B swizzle for the rope part);
+//   2. GEMM1 on the tensor core: S_c[128 x 64] = Q_c (TMEM, A operand) .
+//      K_c^T (smem), 18 k-steps of 16, fp32 accumulate in TMEM;
+//   3. the softmax warps swap partial S through distributed shared memory and
+//      add them (S_0 + S_1 is bit-identical on both CTAs), apply the tree mask
+//      (prefix always visible, tree columns from custom_mask), and run the
+//      fp32 online softmax ("Design Decisions and Trade-Offs": mask -> -inf,
+//      streaming max/sum) with a lazily moved reference max;
+//   4. GEMM2: O_c[128 x 256] += P (bf16, smem) . V_c, where V_c is this CTA's
+//      256 latent dims of the same smem tile read as an MN-major operand.
+// Both CTAs take identical softmax decisions, so O_0 and O_1 are the two
+// halves of one consistent output.  The end of a split writes the normalised
+// partial O and its LSE (or the final bf16 output when there is one split).
+//
+// TMEM (512 columns): O half [0,256), partial S [256,320), Q half [320,464).
+// Every wait is bounded: a timeout sets MTV_DEVERR_TIMEOUT and the CTA winds
+// down (its MMAs and copies drain, TMEM is freed) instead of hanging.
+#include <math.h>
+
 #include "mtv_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace mtv {
 
 extern const int kTcRowTile = 128;
 extern const int kTcKeyTile = 64;
 
-int choose_nsplit_tc(int num_sms, int64_t pairs_per_split, int64_t max_keys, int64_t rows_total) {
-  (void)rows_total;
-  if (pairs_per_split <= 0) return 1;
-  int64_t pairs = num_sms / 2;
-  int64_t want = (pairs + pairs_per_split - 1) / pairs_per_split;
-  int64_t cap = (max_keys + 255) / 256;
-  if (want > cap) want = cap;
-  return int(want < 1 ? 1 : want);
+namespace {
+
+using namespace ptx;
+
+constexpr int ROWS = 128;   // query rows per CTA pair
+constexpr int NK = 64;      // keys per tile
+constexpr int STAGES = 4;   // gather pipeline depth
+constexpr int NPROD_WARPS = 3;
+constexpr int NSOFT_WARPS = 8;  // two per TMEM lane quarter, 32 key columns each
+constexpr int NTHREADS = 32 * (1 + NPROD_WARPS + NSOFT_WARPS);  // warp 0 MMA, 1-3 gather, 4-11 softmax
+constexpr int KSTEPS1 = (256 + 32) / 16;  // 18
+constexpr int KSTEPS2 = NK / 16;          // 4
+constexpr float kRescaleLog2 = 8.0f;      // move the reference max only past 2^8 growth
+constexpr long long kTimeoutCycles = 1ll << 31;
+
+constexpr uint32_t kChunkBytes = NK * 128;                       // 64 latent dims x 64 keys
+constexpr uint32_t kRopeBytes = NK * 64;                          // 32 rope dims x 64 keys
+constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;    // 36 KB
+constexpr uint32_t kOffStages = 0;
+constexpr uint32_t kOffP = kOffStages + STAGES * kStageBytes;    // P tile, bf16 K-major
+constexpr uint32_t kPBytes = ROWS * NK * 2;
+constexpr uint32_t kOffSx = kOffP + kPBytes;                      // peer's partial S
+constexpr uint32_t kSxBytes = ROWS * NK * 4;
+constexpr uint32_t kOffSlots = kOffSx + kSxBytes;                 // key validity bit masks
+constexpr uint32_t kSlotBytes = STAGES * 4 * 8;                 // per stage: 3 validity masks (+pad)
+constexpr uint32_t kOffRowMax = kOffSlots + kSlotBytes;           // [2 tiles][2 halves][128 rows] f32
+constexpr uint32_t kRowMaxBytes = 2 * 2 * ROWS * 4;
+constexpr uint32_t kOffLsum = kOffRowMax + kRowMaxBytes;          // [2 sums][128 rows] f32 (half 1)
+constexpr uint32_t kLsumBytes = 2 * ROWS * 4;
+constexpr uint32_t kOffBars = kOffLsum + kLsumBytes;
+constexpr uint32_t kOffCtl = kOffBars + 256;
+constexpr uint32_t kSmemBytes = kOffCtl + 64 + 1024;  // + slack for 1 KB alignment
+
+constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 320;
+
+enum : int {
+  B_KV_FULL = 0, B_KV_EMPTY = STAGES, B_S_FULL = 2 * STAGES, B_S_FREE, B_P_FULL, B_O_READY, B_Q_READY,
+  B_SX_FULL, B_SX_FREE, B_FIN, B_QMAX, B_COUNT = B_QMAX + 4
+};
+static_assert(B_COUNT * 8 <= 256, "barrier area");
+static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+
+struct Ctl {
+  uint32_t tmem_base;
+  volatile int abort;
+};
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
-cudaError_t prepare_partial_tc() { return cudaSuccess; }
+// Bounded wait on a CTA barrier; false (and abort) on timeout or abort.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl, unsigned* err, bool cluster) {
+  if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  for (;;) {
+    if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (ctl->abort) return false;
+    if (clock64() - t0 > kTimeoutCycles) {
+      ctl->abort = 1;
+      atomicOr(err, MTV_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params P) {
+  extern __shared__ unsigned char smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  unsigned char* gbase = smem_raw + (base - raw);
+  Ctl* ctl = reinterpret_cast<Ctl*>(gbase + kOffCtl);
+  auto bar = [&](int i) { return base + kOffBars + 8u * uint32_t(i); };
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t crank = cluster_ctarank();
+  const uint32_t peer = crank ^ 1u;
+  const int pair = blockIdx.x >> 1;
+  const int r = pair / P.grid_rows, rb = pair % P.grid_rows;
+  const int split = blockIdx.y;
+  const Req R = load_req(P, r);
+  const int64_t rows_req = R.n * kHeads;
+  if (int64_t(rb) * ROWS >= rows_req) return;  // both CTAs of the pair take this exit
+  const int64_t k_begin = int64_t(split) * P.split_keys;
+  if (split > 0 && k_begin >= R.keys) return;  // empty split: the combine never reads it
+  const int64_t k_end = min(R.keys, k_begin + P.split_keys);
+  const int T = int((k_end - k_begin + NK - 1) / NK);
+  uint64_t* vmask_all = reinterpret_cast<uint64_t*>(gbase + kOffSlots);  // [stage][4]
+
+  if (tid == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(bar(B_KV_FULL + s), NPROD_WARPS);
+      mbar_init(bar(B_KV_EMPTY + s), 1);
+    }
+    mbar_init(bar(B_S_FULL), 1);
+    mbar_init(bar(B_S_FREE), NSOFT_WARPS);
+    mbar_init(bar(B_P_FULL), NSOFT_WARPS);
+    mbar_init(bar(B_O_READY), 1);
+    mbar_init(bar(B_Q_READY), NSOFT_WARPS);
+    mbar_init(bar(B_SX_FULL), NSOFT_WARPS);
+    mbar_init(bar(B_SX_FREE), NSOFT_WARPS);
+    mbar_init(bar(B_FIN), 1);
+    for (int qq = 0; qq < 4; ++qq) mbar_init(bar(B_QMAX + qq), 2);
+    ctl->abort = 0;
+    fence_mbar_init_cluster();
+  }
+  if (warp == 0) {
+    tmem_alloc(smem_u32(&ctl->tmem_base), 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();  // barriers of both CTAs initialised before any remote access
+  const uint32_t tmem = ctl->tmem_base;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t id1 = idesc_bf16_f32(128, NK, 0, 0);
+      const uint32_t id2 = idesc_bf16_f32(128, 256, 0, 1);
+      auto gemm2 = [&](int jj) -> bool {
+        if (!wait_bar(bar(B_P_FULL), jj & 1, ctl, P.err, false)) return false;
+        tc_fence_after();
+        const uint32_t st = base + kOffStages + uint32_t(jj % STAGES) * kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS2; ++kk) {
+          const uint64_t ad = smem_desc(base + kOffP + kk * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = smem_desc(st + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
+          mma_ss(tmem + kTmemO, ad, bd, id2, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(B_O_READY));
+        mma_commit(bar(B_KV_EMPTY + jj % STAGES));
+        return true;
+      };
+      bool ok = wait_bar(bar(B_Q_READY), 0, ctl, P.err, false);
+      for (int j = 0; ok && j < T; ++j) {
+        const int s = j % STAGES;
+        ok = wait_bar(bar(B_KV_FULL + s), (j / STAGES) & 1, ctl, P.err, false);
+        if (ok && j > 0) ok = wait_bar(bar(B_S_FREE), (j - 1) & 1, ctl, P.err, false);
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t st = base + kOffStages + uint32_t(s) * kStageBytes;
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS1; ++kk) {
+          const uint64_t bd = kk < 16 ? smem_desc(st + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024, kSwizzle128B)
+                                      : smem_desc(st + 4 * kChunkBytes + (kk - 16) * 32, 16, 512, kSwizzle64B);
+          mma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(B_S_FULL));
+        if (j > 0) ok = gemm2(j - 1);
+      }
+      if (ok) gemm2(T - 1);
+      mma_commit(bar(B_FIN));  // drains every MMA issued above
+      wait_bar(bar(B_FIN), 0, ctl, P.err, false);
+    }
+    __syncwarp();
+  } else if (warp <= NPROD_WARPS) {
+    // ------------------------------------------------------------ gather
+    // Warp pw copies keys pw, pw+3, ... of each tile: lane i first resolves the
+    // slot of the warp's i-th key (all index loads in flight together), then
+    // the warp copies one key at a time, 32 lanes x 16 B of latent + 4 x 16 B
+    // of rope, straight into the swizzled operand layout.
+    const int pw = warp - 1;
+    const int nmine = (NK - pw + NPROD_WARPS - 1) / NPROD_WARPS;  // 22, 21, 21
+    int issued = 0;
+    for (int j = 0; j < T; ++j) {
+      const int s = j % STAGES;
+      const int64_t kt = k_begin + int64_t(j) * NK;
+      int64_t my_slot = -1;
+      if (lane < nmine) {
+        const int64_t k = kt + pw + NPROD_WARPS * lane;
+        if (k < k_end) my_slot = key_slot(P, R, k);
+      }
+      const uint32_t vlo = __reduce_or_sync(0xffffffffu, (my_slot >= 0 && pw + NPROD_WARPS * lane < 32)
+                                                             ? 1u << (pw + NPROD_WARPS * lane) : 0u);
+      const uint32_t vhi = __reduce_or_sync(0xffffffffu, (my_slot >= 0 && pw + NPROD_WARPS * lane >= 32 &&
+                                                          lane < nmine)
+                                                             ? 1u << (pw + NPROD_WARPS * lane - 32) : 0u);
+      if (j >= STAGES) {
+        bool ok = wait_bar(bar(B_KV_EMPTY + s), ((j / STAGES) - 1) & 1, ctl, P.err, false);
+        if (!__all_sync(0xffffffffu, ok)) break;
+      }
+      const uint32_t st = base + kOffStages + uint32_t(s) * kStageBytes;
+      if (lane == 0) vmask_all[s * 4 + pw] = (uint64_t(vhi) << 32) | vlo;
+      for (int i = 0; i < nmine; ++i) {
+        const int kk = pw + NPROD_WARPS * i;
+        const int64_t slot = __shfl_sync(0xffffffffu, my_slot, i);
+        const uint32_t lat = st + uint32_t(lane >> 3) * kChunkBytes + kk * 128 + (((lane & 7) ^ (kk & 7)) << 4);
+        const uint32_t rope = st + 4 * kChunkBytes + kk * 64 + (((lane & 3) ^ ((kk >> 1) & 3)) << 4);
+        if (slot >= 0) {
+          const unsigned char* src = reinterpret_cast<const unsigned char*>(P.kv_pool + slot * kDQK);
+          cp_async_16(lat, src + crank * 512 + lane * 16);
+          if (lane < 4) cp_async_16(rope, src + 1024 + crank * 64 + lane * 16);
+        } else {
+          st_shared_v4(lat, 0u, 0u, 0u, 0u);
+          if (lane < 4) st_shared_v4(rope, 0u, 0u, 0u, 0u);
+        }
+      }
+      cp_async_commit();
+      if (j > 0) {
+        cp_async_wait<1>();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_KV_FULL + (j - 1) % STAGES));
+      }
+      issued = j + 1;
+    }
+    cp_async_wait<0>();
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (issued == T && lane == 0) mbar_arrive(bar(B_KV_FULL + (T - 1) % STAGES));
+  } else {
+    // ------------------------------------------------------------ softmax / epilogue
+    const int sw = warp - 1 - NPROD_WARPS;         // 0..7
+    const int q = warp & 3;                        // TMEM lane quarter this warp may access
+    const int h = sw >> 2;                         // key columns [32h, 32h+32), O columns [128h, +128)
+    const int rr = q * 32 + lane;                  // row within the pair tile = TMEM lane
+    const int64_t grow = int64_t(rb) * ROWS + rr;  // row within the request
+    const bool valid = grow < rows_req;
+    const int64_t ti = grow / kHeads;              // tree token of this row
+    const uint32_t lane_off = uint32_t(q * 32) << 16;
+    const int64_t out_row = R.q_off * kHeads + grow;  // (token, head) row of q/out/lse
+    const uint32_t qbar = bar(B_QMAX + q);            // meeting point of the two warps of this quarter
+    float* rowmax = reinterpret_cast<float*>(gbase + kOffRowMax);  // [tile&1][half][row]
+    float* lsum_s = reinterpret_cast<float*>(gbase + kOffLsum);    // [2][row] from half 1
+
+    // Q half -> TMEM (A operand of GEMM1): column c packs dims (2c, 2c+1); the
+    // two warps of a quarter take alternate 16-column chunks.
+    {
+      const __nv_bfloat16* qrow = P.q + out_row * kDQK;
+#pragma unroll 1
+      for (int c0 = 16 * h; c0 < 144; c0 += 32) {
+        uint32_t v[16];
+        if (valid) {
+          const uint4* src = c0 < 128 ? reinterpret_cast<const uint4*>(qrow + crank * 256 + 2 * c0)
+                                      : reinterpret_cast<const uint4*>(qrow + 512 + crank * 32 + 2 * (c0 - 128));
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const uint4 x = __ldg(src + u);
+            v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+          }
+        } else {
+#pragma unroll
+          for (int u = 0; u < 16; ++u) v[u] = 0u;
+        }
+        tmem_st16_sync(tmem + lane_off + kTmemQ + c0, v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_Q_READY));
+    }
+
+    const uint32_t sx_peer = mapa(base + kOffSx, peer) + uint32_t(rr) * 256u;
+    const uint32_t peer_sx_full = mapa(bar(B_SX_FULL), peer);
+    const uint32_t peer_sx_free = mapa(bar(B_SX_FREE), peer);
+    const float4* sx_mine = reinterpret_cast<const float4*>(gbase + kOffSx + rr * 256);
+    float m_ref = -INFINITY, l_bf = 0.f, l_true = 0.f;
+    bool alive = true;
+
+    for (int j = 0; j < T; ++j) {
+      bool ok = wait_bar(bar(B_S_FULL), j & 1, ctl, P.err, false);
+      if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+      tc_fence_after();
+      uint32_t s[32];
+      tmem_ld32_sync(tmem + lane_off + kTmemS + 32 * h, s);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_S_FREE));
+      // swap partial scores with the peer CTA (this warp's 32 columns)
+      if (j > 0) {
+        ok = wait_bar(bar(B_SX_FREE), (j - 1) & 1, ctl, P.err, true);
+        if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+      }
+#pragma unroll
+      for (int u = 0; u < 8; ++u)
+        st_cluster_v4(sx_peer + ((uint32_t(8 * h + u) ^ uint32_t(rr & 15)) << 4), s[4 * u], s[4 * u + 1],
+                      s[4 * u + 2], s[4 * u + 3]);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(peer_sx_full);
+      ok = wait_bar(bar(B_SX_FULL), j & 1, ctl, P.err, true);
+      if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+      float x[32];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const float4 v = sx_mine[(8 * h + u) ^ (rr & 15)];
+        x[4 * u] = __uint_as_float(s[4 * u]) + v.x;
+        x[4 * u + 1] = __uint_as_float(s[4 * u + 1]) + v.y;
+        x[4 * u + 2] = __uint_as_float(s[4 * u + 2]) + v.z;
+        x[4 * u + 3] = __uint_as_float(s[4 * u + 3]) + v.w;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(peer_sx_free);
+
+      // mask + scale (log2 domain)
+      const int sidx = j % STAGES;
+      ok = wait_bar(bar(B_KV_FULL + sidx), (j / STAGES) & 1, ctl, P.err, false);
+      if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+      const uint64_t vm = vmask_all[sidx * 4] | vmask_all[sidx * 4 + 1] | vmask_all[sidx * 4 + 2];
+      const uint32_t vbits = uint32_t(vm >> (32 * h));
+      const int64_t kt = k_begin + int64_t(j) * NK + 32 * h;  // global key of column 0 of this warp
+      float mt = -INFINITY;
+      if (valid && vbits == 0xffffffffu && kt + 32 <= R.p) {  // all prefix keys, all resolved
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          x[c] *= P.scale_log2;
+          mt = fmaxf(mt, x[c]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          const int64_t k = kt + c;
+          bool vis = valid && ((vbits >> c) & 1u);
+          if (vis && k >= R.p) vis = tree_visible(P, R, ti, k - R.p);
+          x[c] = vis ? x[c] * P.scale_log2 : -INFINITY;
+          mt = fmaxf(mt, x[c]);
+        }
+      }
+      // combine the tile max of the two halves of this row (bounded mbarrier meeting)
+      rowmax[((j & 1) * 2 + h) * ROWS + rr] = mt;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qbar);
+      ok = wait_bar(qbar, j & 1, ctl, P.err, false);
+      if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+      mt = fmaxf(mt, rowmax[((j & 1) * 2 + (h ^ 1)) * ROWS + rr]);
+
+      const float m_new = fmaxf(m_ref, mt);
+      const bool move = (m_new > m_ref + kRescaleLog2) || (m_ref == -INFINITY && m_new != -INFINITY);
+      const float fac = move ? ex2(m_ref - m_new) : 1.f;  // ex2(-inf) = 0
+
+      if (j > 0) {
+        ok = wait_bar(bar(B_O_READY), (j - 1) & 1, ctl, P.err, false);
+        if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, move)) {  // warp-uniform TMEM read-modify-write of this warp's O half
+#pragma unroll 1
+          for (int c0 = 128 * h; c0 < 128 * h + 128; c0 += 32) {
+            uint32_t v[32];
+            tmem_ld32_sync(tmem + lane_off + kTmemO + c0, v);
+#pragma unroll
+            for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * fac);
+            tmem_st32_sync(tmem + lane_off + kTmemO + c0, v);
+          }
+        }
+      }
+      if (move) {
+        l_bf *= fac;
+        l_true *= fac;
+        m_ref = m_new;
+      }
+      const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float sb = 0.f, st = 0.f;
+      uint32_t pk[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const float p0 = ex2(x[2 * u] - mref), p1 = ex2(x[2 * u + 1] - mref);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
+        const float2 f = __bfloat1622float2(b);
+        sb += f.x + f.y;   // what the tensor core multiplies: normalises O
+        st += p0 + p1;     // unrounded weights: the LSE
+        pk[u] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      l_bf += sb;
+      l_true += st;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        st_shared_v4(base + kOffP + uint32_t(rr) * 128u + ((uint32_t(4 * h + u) ^ uint32_t(rr & 7)) << 4),
+                     pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
+      fence_proxy_async_smem();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(B_P_FULL));
+    }
+
+    // epilogue: normalised O half (+ LSE from CTA 0)
+    if (alive) {
+      bool ok = wait_bar(bar(B_O_READY), (T - 1) & 1, ctl, P.err, false);
+      alive = __all_sync(0xffffffffu, ok);
+    }
+    // the row's two partial sums (one per half) meet in shared memory: half 1
+    // publishes, half 0 adds and publishes the totals, half 1 reads them back
+    if (alive) {
+      if (h == 1) {
+        lsum_s[rr] = l_bf;
+        lsum_s[ROWS + rr] = l_true;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qbar);
+      bool ok = wait_bar(qbar, T & 1, ctl, P.err, false);
+      alive = __all_sync(0xffffffffu, ok);
+    }
+    if (alive) {
+      if (h == 0) {
+        lsum_s[rr] += l_bf;
+        lsum_s[ROWS + rr] += l_true;
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(qbar);
+      bool ok = wait_bar(qbar, (T + 1) & 1, ctl, P.err, false);
+      alive = __all_sync(0xffffffffu, ok);
+    }
+    if (alive) {
+      const float tot_bf = lsum_s[rr], tot_true = lsum_s[ROWS + rr];
+      tc_fence_after();
+      const float inv = tot_bf > 0.f ? 1.f / tot_bf : 0.f;
+#pragma unroll 1
+      for (int c0 = 128 * h; c0 < 128 * h + 128; c0 += 32) {
+        uint32_t v[32];
+        tmem_ld32_sync(tmem + lane_off + kTmemO + c0, v);
+        if (!valid) continue;
+        const int dcol = int(crank) * 256 + c0;
+        if (P.nsplit == 1) {
+          uint4* dst = reinterpret_cast<uint4*>(P.out + out_row * kDLat + dcol);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            uint32_t w[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[8 * u + 2 * e]) * inv,
+                                                             __uint_as_float(v[8 * u + 2 * e + 1]) * inv);
+              w[e] = *reinterpret_cast<const uint32_t*>(&b);
+            }
+            dst[u] = make_uint4(w[0], w[1], w[2], w[3]);
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(
+              P.part_o + (int64_t(split) * P.total_q_max * kHeads + out_row) * kDLat + dcol);
+#pragma unroll
+          for (int u = 0; u < 8; ++u)
+            dst[u] = make_float4(__uint_as_float(v[4 * u]) * inv, __uint_as_float(v[4 * u + 1]) * inv,
+                                 __uint_as_float(v[4 * u + 2]) * inv, __uint_as_float(v[4 * u + 3]) * inv);
+        }
+      }
+      if (valid && crank == 0 && h == 0) {
+        const float lse = tot_true > 0.f ? (m_ref + __log2f(tot_true)) * kLn2 : -INFINITY;
+        if (P.nsplit == 1) P.lse[out_row] = lse;
+        else P.part_lse[int64_t(split) * P.total_q_max * kHeads + out_row] = lse;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 0) tmem_dealloc(tmem, 512);
+  cluster_sync();  // the peer may still arrive on / store into this CTA's shared memory until here
+}
+
+}  // namespace
+
+// Split count for the tensor-core kernel: fill the SM pairs in whole waves
+// while keeping the fp32 partial traffic of the combine small.
+int choose_nsplit_tc(int num_sms, int64_t pairs_per_split, int64_t max_keys, int64_t rows_total) {
+  if (pairs_per_split <= 0) return 1;
+  const double slots = double(num_sms / 2);
+  const double t_key_us = 0.02;     // one 64-key tile costs ~1.3 us per pair; per key
+  const double t_fixed_us = 4.0;    // launch, Q load, pipeline fill, epilogue
+  const double hbm_bytes_per_us = 6.0e6;
+  int best = 1;
+  double best_t = 1e30;
+  for (int ns = 1; ns <= 64; ++ns) {
+    const double keys = double(((max_keys + ns - 1) / ns + NK - 1) / NK * NK);
+    if (ns > 1 && keys * (ns - 1) >= double(max_keys) + NK) break;  // last split would be empty
+    const double waves = ceil(double(pairs_per_split) * ns / slots);
+    double t = waves * (keys * t_key_us + t_fixed_us);
+    if (ns > 1) t += double(ns) * double(rows_total) * kDLat * 4.0 * 2.0 / hbm_bytes_per_us + 2.0;
+    if (t < best_t * 0.98) {
+      best_t = t;
+      best = ns;
+    }
+  }
+  return best;
+}
+
+cudaError_t prepare_partial_tc() {
+  return cudaFuncSetAttribute(partial_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, int(kSmemBytes));
+}
 
 cudaError_t launch_partial_tc(const Params& P, cudaStream_t st) {
-  (void)P; (void)st;
-  return cudaErrorNotSupported;
+  const int64_t pairs = int64_t(P.bs) * P.grid_rows;
+  if (pairs == 0) return cudaSuccess;
+  dim3 grid(unsigned(2 * pairs), unsigned(P.nsplit));
+  partial_tc_kernel<<<grid, NTHREADS, kSmemBytes, st>>>(P);
+  return cudaGetLastError();
 }
 
 }  // namespace mtv
