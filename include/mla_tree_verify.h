@@ -50,7 +50,7 @@ extern "C" {
 #define MTV_OK 0
 #define MTV_E_NULL_POINTER -1      /* a required pointer is NULL                   */
 #define MTV_E_UNSUPPORTED -2       /* H != 64, d_latent != 512 or d_rope != 64      */
-#define MTV_E_BAD_ARGUMENT -3      /* negative sizes, unknown mask layout or flags  */
+#define MTV_E_BAD_ARGUMENT -3      /* bad size, alignment, mask layout or flags     */
 #define MTV_E_WORKSPACE_SMALL -4   /* workspace_bytes < plan->ws_bytes              */
 #define MTV_E_WORKSPACE_ALIGN -5   /* workspace not 256-byte aligned                */
 #define MTV_E_BAD_PLAN -6          /* plan not produced by mla_tree_verify_plan     */
@@ -127,8 +127,10 @@ int mla_tree_verify_plan(int device, int bs, int max_q_per_req, int64_t total_q_
  * mla_tree_verify_run -- enqueue one verify-attention pass on `stream`.
  *
  * q              device, bf16 [total_q, 64, 576] row-major (token, head, dim).
- * kv_pool        device, bf16 [num_slots, 576]; V is columns 0..511 of each row.
- * num_slots      rows in kv_pool (slot indices are checked against it).
+ * kv_pool        device, bf16 [num_slots, 576], 16-byte aligned; V is columns
+ *                0..511 of each row.
+ * num_slots      rows in kv_pool, 0 <= num_slots < 2^31 (slot indices are
+ *                checked against it; an out-of-range slot is treated as masked).
  * kv_indices     device, int64 [kv_indptr[bs]]: prefix slots, request-major.
  * kv_indptr      device, int32 [bs + 1]: CSR offsets into kv_indices.
  * out_cache_loc  device, int64 [qo_indptr[bs]]: slot of every tree token.

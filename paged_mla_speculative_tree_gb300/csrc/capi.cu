@@ -153,7 +153,8 @@ int mla_tree_verify_run(const mtv_plan_t* plan, const void* q, const void* kv_po
   if (plan->bs > 0 && plan->total_q_max > 0 &&
       (!q || !kv_pool || !kv_indices || !out_cache_loc || !custom_mask || !out || !lse))
     return MTV_E_NULL_POINTER;
-  if (num_slots < 0) return MTV_E_BAD_ARGUMENT;
+  if (num_slots < 0 || num_slots > INT32_MAX) return MTV_E_BAD_ARGUMENT;  // TMA row coordinates are 32-bit
+  if (reinterpret_cast<uintptr_t>(kv_pool) & 15) return MTV_E_BAD_ARGUMENT;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return MTV_E_WORKSPACE_ALIGN;
   if (workspace_bytes < plan->ws_bytes) return MTV_E_WORKSPACE_SMALL;
   int cur = -1;

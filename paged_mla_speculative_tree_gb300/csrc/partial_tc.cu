@@ -11,24 +11,35 @@
 //
 // The 576 contraction dims are split between the two CTAs: CTA c holds latent
 // dims [256c, 256c+256) and rope dims [32c, 32c+32).  Per 64-key tile:
-//   1. producers gather the CTA's 576 bytes of each latent row with cp.async
-//      into a 128B-swizzled K-major tile (64B swizzle for the rope part);
+//   1. seven gather warps copy the CTA's 576 bytes of each latent row with
+//      cp.async (16 B per lane, one row per warp instruction) into a
+//      128B-swizzled K-major tile (64B swizzle for the rope part); invalid
+//      slots are zero-filled; each lane's copies complete on the stage's
+//      barrier, so the warps never wait for memory.  (Scattered 1152-byte
+//      rows: per-warp cp.async scales with the number of issuing warps, while
+//      TMA gathers are limited to about one 128-byte row per 18 cycles per SM);
 //   2. GEMM1 on the tensor core: S_c[128 x 64] = Q_c (TMEM, A operand) .
 //      K_c^T (smem), 18 k-steps of 16, fp32 accumulate in TMEM;
-//   3. the softmax warps swap partial S through distributed shared memory and
-//      add them (S_0 + S_1 is bit-identical on both CTAs), apply the tree mask
-//      (prefix always visible, tree columns from custom_mask), and run the
-//      fp32 online softmax ("Design Decisions and Trade-Offs": mask -> -inf,
-//      streaming max/sum) with a lazily moved reference max;
-//   4. GEMM2: O_c[128 x 256] += P (bf16, smem) . V_c, where V_c is this CTA's
-//      256 latent dims of the same smem tile read as an MN-major operand.
+//   3. the softmax warps send their partial S to the peer CTA with st.async
+//      (completing bytes on the peer's barrier, double-buffered, one tile
+//      ahead), add the peer's partial (S_0 + S_1 is bit-identical on both
+//      CTAs), apply the tree mask (prefix always visible, tree columns from
+//      custom_mask), and run the fp32 online softmax ("Design Decisions and
+//      Trade-Offs": mask -> -inf, streaming max/sum) with a lazily moved
+//      reference max; P (bf16) goes to TMEM;
+//   4. GEMM2: O_c[128 x 256] += P (TMEM, A operand) . V_c, where V_c is this
+//      CTA's 256 latent dims of the same smem tile read as an MN-major operand.
 // Both CTAs take identical softmax decisions, so O_0 and O_1 are the two
 // halves of one consistent output.  The end of a split writes the normalised
 // partial O and its LSE (or the final bf16 output when there is one split).
 //
-// TMEM (512 columns): O half [0,256), partial S [256,320), Q half [320,464).
-// Every wait is bounded: a timeout sets MTV_DEVERR_TIMEOUT and the CTA winds
-// down (its MMAs and copies drain, TMEM is freed) instead of hanging.
+// TMEM (512 columns): O half [0,256), partial S [256,320), Q half [320,464),
+// P [464,496).  Every wait is bounded: a timeout sets MTV_DEVERR_TIMEOUT and
+// the CTA winds down (its MMAs and copies drain, TMEM is freed) instead of
+// hanging.
+//
+// Building with -DMTV_TRACE records clock64() timestamps of the pipeline
+// events of the first CTA into a device buffer (read with mtv_trace_read).
 #include <math.h>
 
 #include "mtv_internal.cuh"
@@ -46,9 +57,9 @@ using namespace ptx;
 constexpr int ROWS = 128;   // query rows per CTA pair
 constexpr int NK = 64;      // keys per tile
 constexpr int STAGES = 4;   // gather pipeline depth
-constexpr int NPROD_WARPS = 3;
+constexpr int NPROD_WARPS = 7;
 constexpr int NSOFT_WARPS = 8;  // two per TMEM lane quarter, 32 key columns each
-constexpr int NTHREADS = 32 * (1 + NPROD_WARPS + NSOFT_WARPS);  // warp 0 MMA, 1-3 gather, 4-11 softmax
+constexpr int NTHREADS = 32 * (1 + NPROD_WARPS + NSOFT_WARPS);  // warp 0 MMA, 1-7 gather, 8-15 softmax
 constexpr int KSTEPS1 = (256 + 32) / 16;  // 18
 constexpr int KSTEPS2 = NK / 16;          // 4
 constexpr float kRescaleLog2 = 8.0f;      // move the reference max only past 2^8 growth
@@ -58,25 +69,23 @@ constexpr uint32_t kChunkBytes = NK * 128;                       // 64 latent di
 constexpr uint32_t kRopeBytes = NK * 64;                          // 32 rope dims x 64 keys
 constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;    // 36 KB
 constexpr uint32_t kOffStages = 0;
-constexpr uint32_t kOffP = kOffStages + STAGES * kStageBytes;    // P tile, bf16 K-major
-constexpr uint32_t kPBytes = ROWS * NK * 2;
-constexpr uint32_t kOffSx = kOffP + kPBytes;                      // peer's partial S
+constexpr uint32_t kOffSx = kOffStages + STAGES * kStageBytes;   // peer's partial S, 2 buffers
 constexpr uint32_t kSxBytes = ROWS * NK * 4;
-constexpr uint32_t kOffSlots = kOffSx + kSxBytes;                 // key validity bit masks
-constexpr uint32_t kSlotBytes = STAGES * 4 * 8;                 // per stage: 3 validity masks (+pad)
-constexpr uint32_t kOffRowMax = kOffSlots + kSlotBytes;           // [2 tiles][2 halves][128 rows] f32
+constexpr uint32_t kOffVmask = kOffSx + 2 * kSxBytes;             // key validity bit masks
+constexpr uint32_t kVmaskBytes = STAGES * 8 * 8;  // [stage][gather warp] partial masks
+constexpr uint32_t kOffRowMax = kOffVmask + kVmaskBytes;          // [2 tiles][2 halves][128 rows] f32
 constexpr uint32_t kRowMaxBytes = 2 * 2 * ROWS * 4;
-constexpr uint32_t kOffLsum = kOffRowMax + kRowMaxBytes;          // [2 sums][128 rows] f32 (half 1)
+constexpr uint32_t kOffLsum = kOffRowMax + kRowMaxBytes;          // [2 sums][128 rows] f32
 constexpr uint32_t kLsumBytes = 2 * ROWS * 4;
 constexpr uint32_t kOffBars = kOffLsum + kLsumBytes;
 constexpr uint32_t kOffCtl = kOffBars + 256;
 constexpr uint32_t kSmemBytes = kOffCtl + 64 + 1024;  // + slack for 1 KB alignment
 
-constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 320;
+constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 320, kTmemP = 464;
 
 enum : int {
   B_KV_FULL = 0, B_KV_EMPTY = STAGES, B_S_FULL = 2 * STAGES, B_S_FREE, B_P_FULL, B_O_READY, B_Q_READY,
-  B_SX_FULL, B_SX_FREE, B_FIN, B_QMAX, B_COUNT = B_QMAX + 4
+  B_SX_FULL0, B_SX_FULL1, B_FIN, B_QMAX, B_COUNT = B_QMAX + 4
 };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
@@ -85,6 +94,19 @@ struct Ctl {
   uint32_t tmem_base;
   volatile int abort;
 };
+
+#ifdef MTV_TRACE
+constexpr int kTraceTiles = 128, kTraceEvents = 16;
+__device__ long long g_trace[4][kTraceTiles][kTraceEvents];
+#define MTV_TR(role, tile, ev)                                                                            \
+  do {                                                                                                    \
+    if (blockIdx.x == 0 && blockIdx.y == 0 && (tile) < kTraceTiles) g_trace[role][tile][ev] = clock64(); \
+  } while (0)
+#else
+#define MTV_TR(role, tile, ev) \
+  do {                         \
+  } while (0)
+#endif
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -128,11 +150,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
   if (split > 0 && k_begin >= R.keys) return;  // empty split: the combine never reads it
   const int64_t k_end = min(R.keys, k_begin + P.split_keys);
   const int T = int((k_end - k_begin + NK - 1) / NK);
-  uint64_t* vmask_all = reinterpret_cast<uint64_t*>(gbase + kOffSlots);  // [stage][4]
+  uint64_t* vmask_all = reinterpret_cast<uint64_t*>(gbase + kOffVmask);  // [stage][8]
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
-      mbar_init(bar(B_KV_FULL + s), NPROD_WARPS);
+      mbar_init(bar(B_KV_FULL + s), NPROD_WARPS * 33);  // 32 copy completions + 1 mask arrival per warp
       mbar_init(bar(B_KV_EMPTY + s), 1);
     }
     mbar_init(bar(B_S_FULL), 1);
@@ -140,8 +162,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     mbar_init(bar(B_P_FULL), NSOFT_WARPS);
     mbar_init(bar(B_O_READY), 1);
     mbar_init(bar(B_Q_READY), NSOFT_WARPS);
-    mbar_init(bar(B_SX_FULL), NSOFT_WARPS);
-    mbar_init(bar(B_SX_FREE), NSOFT_WARPS);
+    mbar_init(bar(B_SX_FULL0), 1);  // one local expect_tx arrival + the peer's st.async bytes
+    mbar_init(bar(B_SX_FULL1), 1);
     mbar_init(bar(B_FIN), 1);
     for (int qq = 0; qq < 4; ++qq) mbar_init(bar(B_QMAX + qq), 2);
     ctl->abort = 0;
@@ -164,24 +186,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       const uint32_t id2 = idesc_bf16_f32(128, 256, 0, 1);
       auto gemm2 = [&](int jj) -> bool {
         if (!wait_bar(bar(B_P_FULL), jj & 1, ctl, P.err, false)) return false;
+        MTV_TR(0, jj, 2);
         tc_fence_after();
         const uint32_t st = base + kOffStages + uint32_t(jj % STAGES) * kStageBytes;
 #pragma unroll
         for (int kk = 0; kk < KSTEPS2; ++kk) {
-          const uint64_t ad = smem_desc(base + kOffP + kk * 32, 16, 1024, kSwizzle128B);
           const uint64_t bd = smem_desc(st + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
-          mma_ss(tmem + kTmemO, ad, bd, id2, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + kTmemO, tmem + kTmemP + kk * 8, bd, id2, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(B_O_READY));
         mma_commit(bar(B_KV_EMPTY + jj % STAGES));
         return true;
       };
+      // GEMM1 of tile j is issued as soon as its stage has landed and the
+      // softmax has read S(j-1); GEMM2 trails by two tiles, so the softmax of
+      // tile j finds S(j+1) already computed when it fetches it.
       bool ok = wait_bar(bar(B_Q_READY), 0, ctl, P.err, false);
       for (int j = 0; ok && j < T; ++j) {
         const int s = j % STAGES;
         ok = wait_bar(bar(B_KV_FULL + s), (j / STAGES) & 1, ctl, P.err, false);
+        MTV_TR(0, j, 0);
         if (ok && j > 0) ok = wait_bar(bar(B_S_FREE), (j - 1) & 1, ctl, P.err, false);
         if (!ok) break;
+        MTV_TR(0, j, 1);
+        fence_proxy_async_smem();  // cp.async wrote the stage through the generic proxy
         tc_fence_after();
         const uint32_t st = base + kOffStages + uint32_t(s) * kStageBytes;
 #pragma unroll
@@ -191,8 +219,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
           mma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(B_S_FULL));
-        if (j > 0) ok = gemm2(j - 1);
+        if (j >= 2) ok = gemm2(j - 2);
       }
+      if (ok && T >= 2) ok = gemm2(T - 2);
       if (ok) gemm2(T - 1);
       mma_commit(bar(B_FIN));  // drains every MMA issued above
       wait_bar(bar(B_FIN), 0, ctl, P.err, false);
@@ -200,59 +229,66 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     __syncwarp();
   } else if (warp <= NPROD_WARPS) {
     // ------------------------------------------------------------ gather
-    // Warp pw copies keys pw, pw+3, ... of each tile: lane i first resolves the
-    // slot of the warp's i-th key (all index loads in flight together), then
-    // the warp copies one key at a time, 32 lanes x 16 B of latent + 4 x 16 B
-    // of rope, straight into the swizzled operand layout.
+    // Warp pw copies keys pw, pw+7, ... of each tile (10 or 9 keys).  Lane i
+    // holds the slot of the warp's i-th key, loaded two tiles ahead and only
+    // checked when used, so index latency never stalls the warp.  Per key the
+    // warp issues one 512-byte latent copy (32 lanes x 16 B) and one 64-byte
+    // rope copy (4 lanes) into the swizzled operand layout; an invalid slot is
+    // zero-filled (source size 0).  Each lane then arrives on the stage's
+    // barrier when its own copies land: the warp only waits for a free stage.
     const int pw = warp - 1;
-    const int nmine = (NK - pw + NPROD_WARPS - 1) / NPROD_WARPS;  // 22, 21, 21
-    int issued = 0;
+    const int nmine = (NK - pw + NPROD_WARPS - 1) / NPROD_WARPS;  // 10 or 9
+    auto raw_slot = [&](int j) -> int64_t {
+      int64_t v = -1;
+      if (lane < nmine && j < T) {
+        const int64_t k = k_begin + int64_t(j) * NK + pw + NPROD_WARPS * lane;
+        if (k < k_end) v = (k < R.p) ? P.kv_indices[R.kv_off + k] : P.out_cache_loc[R.q_off + (k - R.p)];
+      }
+      return v;
+    };
+    int64_t v0 = raw_slot(0), v1 = raw_slot(1);
     for (int j = 0; j < T; ++j) {
       const int s = j % STAGES;
-      const int64_t kt = k_begin + int64_t(j) * NK;
-      int64_t my_slot = -1;
-      if (lane < nmine) {
-        const int64_t k = kt + pw + NPROD_WARPS * lane;
-        if (k < k_end) my_slot = key_slot(P, R, k);
+      int64_t slot = -1;  // checked slot of this lane's key
+      {
+        const int64_t k = k_begin + int64_t(j) * NK + pw + NPROD_WARPS * lane;
+        if (lane < nmine && k < k_end) {
+          if (v0 >= 0 && v0 < P.num_slots) slot = v0;
+          else atomicOr(P.err, MTV_DEVERR_SLOT_RANGE);
+        }
       }
-      const uint32_t vlo = __reduce_or_sync(0xffffffffu, (my_slot >= 0 && pw + NPROD_WARPS * lane < 32)
-                                                             ? 1u << (pw + NPROD_WARPS * lane) : 0u);
-      const uint32_t vhi = __reduce_or_sync(0xffffffffu, (my_slot >= 0 && pw + NPROD_WARPS * lane >= 32 &&
-                                                          lane < nmine)
-                                                             ? 1u << (pw + NPROD_WARPS * lane - 32) : 0u);
+      v0 = v1;
+      v1 = raw_slot(j + 2);  // in flight until two iterations from now
+      const int kk_l = pw + NPROD_WARPS * lane;
+      const uint32_t vlo = __reduce_or_sync(0xffffffffu, (slot >= 0 && kk_l < 32) ? 1u << kk_l : 0u);
+      const uint32_t vhi = __reduce_or_sync(0xffffffffu, (slot >= 0 && kk_l >= 32) ? 1u << (kk_l - 32) : 0u);
       if (j >= STAGES) {
         bool ok = wait_bar(bar(B_KV_EMPTY + s), ((j / STAGES) - 1) & 1, ctl, P.err, false);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
+      if (pw == 0 && lane == 0) MTV_TR(1, j, 0);
       const uint32_t st = base + kOffStages + uint32_t(s) * kStageBytes;
-      if (lane == 0) vmask_all[s * 4 + pw] = (uint64_t(vhi) << 32) | vlo;
+      const uint32_t fb = bar(B_KV_FULL + s);
+      if (lane == 0) {
+        vmask_all[s * 8 + pw] = (uint64_t(vhi) << 32) | vlo;
+        mbar_arrive(fb);  // release: publishes this warp's mask
+      }
+#pragma unroll 2
       for (int i = 0; i < nmine; ++i) {
         const int kk = pw + NPROD_WARPS * i;
-        const int64_t slot = __shfl_sync(0xffffffffu, my_slot, i);
+        const int64_t sl = __shfl_sync(0xffffffffu, slot, i);
         const uint32_t lat = st + uint32_t(lane >> 3) * kChunkBytes + kk * 128 + (((lane & 7) ^ (kk & 7)) << 4);
         const uint32_t rope = st + 4 * kChunkBytes + kk * 64 + (((lane & 3) ^ ((kk >> 1) & 3)) << 4);
-        if (slot >= 0) {
-          const unsigned char* src = reinterpret_cast<const unsigned char*>(P.kv_pool + slot * kDQK);
-          cp_async_16(lat, src + crank * 512 + lane * 16);
-          if (lane < 4) cp_async_16(rope, src + 1024 + crank * 64 + lane * 16);
-        } else {
-          st_shared_v4(lat, 0u, 0u, 0u, 0u);
-          if (lane < 4) st_shared_v4(rope, 0u, 0u, 0u, 0u);
-        }
+        const unsigned char* src = sl >= 0 ? reinterpret_cast<const unsigned char*>(P.kv_pool + sl * kDQK)
+                                           : reinterpret_cast<const unsigned char*>(P.q);
+        const uint32_t nbytes = sl >= 0 ? 16u : 0u;
+        cp_async_16_zfill(lat, src + (sl >= 0 ? crank * 512 + lane * 16 : 0), nbytes);
+        if (lane < 4) cp_async_16_zfill(rope, src + (sl >= 0 ? 1024 + crank * 64 + lane * 16 : 0), nbytes);
       }
-      cp_async_commit();
-      if (j > 0) {
-        cp_async_wait<1>();
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar(B_KV_FULL + (j - 1) % STAGES));
-      }
-      issued = j + 1;
+      cp_async_arrive_noinc(fb);
+      if (pw == 0 && lane == 0) MTV_TR(1, j, 1);
     }
-    cp_async_wait<0>();
-    fence_proxy_async_smem();
-    __syncwarp();
-    if (issued == T && lane == 0) mbar_arrive(bar(B_KV_FULL + (T - 1) % STAGES));
+    cp_async_wait<0>();  // no copy may be in flight when the CTA exits
   } else {
     // ------------------------------------------------------------ softmax / epilogue
     const int sw = warp - 1 - NPROD_WARPS;         // 0..7
@@ -266,7 +302,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     const int64_t out_row = R.q_off * kHeads + grow;  // (token, head) row of q/out/lse
     const uint32_t qbar = bar(B_QMAX + q);            // meeting point of the two warps of this quarter
     float* rowmax = reinterpret_cast<float*>(gbase + kOffRowMax);  // [tile&1][half][row]
-    float* lsum_s = reinterpret_cast<float*>(gbase + kOffLsum);    // [2][row] from half 1
+    float* lsum_s = reinterpret_cast<float*>(gbase + kOffLsum);    // [2][row]
+    const bool tracer = (sw == 0 && lane == 0);
 
     // Q half -> TMEM (A operand of GEMM1): column c packs dims (2c, 2c+1); the
     // two warps of a quarter take alternate 16-column chunks.
@@ -294,54 +331,67 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       if (lane == 0) mbar_arrive(bar(B_Q_READY));
     }
 
+    // Partial-score exchange, double-buffered: the partial of tile j goes to
+    // the peer's buffer j&1 and completes bytes on its barrier SX_FULL(j&1).
+    // A CTA sends tile j+1 only after it has consumed tile j, and it consumed
+    // tile j only after the peer had finished reading tile j-1 (the peer sent
+    // tile j after that read), so buffer (j+1)&1 is always free when written.
     const uint32_t sx_peer = mapa(base + kOffSx, peer) + uint32_t(rr) * 256u;
-    const uint32_t peer_sx_full = mapa(bar(B_SX_FULL), peer);
-    const uint32_t peer_sx_free = mapa(bar(B_SX_FREE), peer);
-    const float4* sx_mine = reinterpret_cast<const float4*>(gbase + kOffSx + rr * 256);
+    const uint32_t peer_sx_full = mapa(bar(B_SX_FULL0), peer);  // + 8 for buffer 1
     float m_ref = -INFINITY, l_bf = 0.f, l_true = 0.f;
     bool alive = true;
+    uint32_t s[32];  // this CTA's partial scores of the tile being finished
 
-    for (int j = 0; j < T; ++j) {
-      bool ok = wait_bar(bar(B_S_FULL), j & 1, ctl, P.err, false);
-      if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+    // load tile jn's partial scores from TMEM and send them to the peer
+    auto fetch_and_send = [&](int jn) -> bool {
+      bool ok = wait_bar(bar(B_S_FULL), jn & 1, ctl, P.err, false);
+      if (!__all_sync(0xffffffffu, ok)) return false;
+      if (tracer) MTV_TR(2, jn, 0);
       tc_fence_after();
-      uint32_t s[32];
       tmem_ld32_sync(tmem + lane_off + kTmemS + 32 * h, s);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_S_FREE));
-      // swap partial scores with the peer CTA (this warp's 32 columns)
-      if (j > 0) {
-        ok = wait_bar(bar(B_SX_FREE), (j - 1) & 1, ctl, P.err, true);
-        if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
-      }
+      const uint32_t dst = sx_peer + uint32_t(jn & 1) * kSxBytes;
+      const uint32_t pbar = peer_sx_full + 8u * uint32_t(jn & 1);
 #pragma unroll
       for (int u = 0; u < 8; ++u)
-        st_cluster_v4(sx_peer + ((uint32_t(8 * h + u) ^ uint32_t(rr & 15)) << 4), s[4 * u], s[4 * u + 1],
-                      s[4 * u + 2], s[4 * u + 3]);
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(peer_sx_full);
-      ok = wait_bar(bar(B_SX_FULL), j & 1, ctl, P.err, true);
+        st_async_v4(dst + ((uint32_t(8 * h + u) ^ uint32_t(rr & 15)) << 4), s[4 * u], s[4 * u + 1], s[4 * u + 2],
+                    s[4 * u + 3], pbar);
+      if (tracer) MTV_TR(2, jn, 1);
+      return true;
+    };
+
+    if (tracer) mbar_arrive_expect_tx(bar(B_SX_FULL0), kSxBytes);  // tile 0
+    alive = fetch_and_send(0);
+    for (int j = 0; alive && j < T; ++j) {
+      // tile j+1's bytes land in buffer (j+1)&1, whose previous phase (tile j-1) is complete
+      if (tracer && j + 1 < T) mbar_arrive_expect_tx(bar(B_SX_FULL0 + ((j + 1) & 1)), kSxBytes);
+      bool ok = wait_bar(bar(B_SX_FULL0 + (j & 1)), (j >> 1) & 1, ctl, P.err, false);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+      if (tracer) MTV_TR(2, j, 2);
       float x[32];
+      {
+        const float4* sx_mine = reinterpret_cast<const float4*>(gbase + kOffSx + (j & 1) * kSxBytes + rr * 256);
 #pragma unroll
-      for (int u = 0; u < 8; ++u) {
-        const float4 v = sx_mine[(8 * h + u) ^ (rr & 15)];
-        x[4 * u] = __uint_as_float(s[4 * u]) + v.x;
-        x[4 * u + 1] = __uint_as_float(s[4 * u + 1]) + v.y;
-        x[4 * u + 2] = __uint_as_float(s[4 * u + 2]) + v.z;
-        x[4 * u + 3] = __uint_as_float(s[4 * u + 3]) + v.w;
+        for (int u = 0; u < 8; ++u) {
+          const float4 v = sx_mine[(8 * h + u) ^ (rr & 15)];
+          x[4 * u] = __uint_as_float(s[4 * u]) + v.x;
+          x[4 * u + 1] = __uint_as_float(s[4 * u + 1]) + v.y;
+          x[4 * u + 2] = __uint_as_float(s[4 * u + 2]) + v.z;
+          x[4 * u + 3] = __uint_as_float(s[4 * u + 3]) + v.w;
+        }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive_cluster(peer_sx_free);
 
       // mask + scale (log2 domain)
       const int sidx = j % STAGES;
       ok = wait_bar(bar(B_KV_FULL + sidx), (j / STAGES) & 1, ctl, P.err, false);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
-      const uint64_t vm = vmask_all[sidx * 4] | vmask_all[sidx * 4 + 1] | vmask_all[sidx * 4 + 2];
+      uint64_t vm = 0;
+#pragma unroll
+      for (int w = 0; w < NPROD_WARPS; ++w) vm |= vmask_all[sidx * 8 + w];
       const uint32_t vbits = uint32_t(vm >> (32 * h));
-      const int64_t kt = k_begin + int64_t(j) * NK + 32 * h;  // global key of column 0 of this warp
+      const int64_t kt = k_begin + int64_t(j) * NK + 32 * h;  // key of this warp's first column
       float mt = -INFINITY;
       if (valid && vbits == 0xffffffffu && kt + 32 <= R.p) {  // all prefix keys, all resolved
 #pragma unroll
@@ -359,22 +409,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
           mt = fmaxf(mt, x[c]);
         }
       }
-      // combine the tile max of the two halves of this row (bounded mbarrier meeting)
+      // The tile max depends on every value read from the exchange buffer, so
+      // once it is stored those reads are complete and tile j+1 may be sent
+      // (the peer writes our buffer j&1 again only after receiving it).
       rowmax[((j & 1) * 2 + h) * ROWS + rr] = mt;
+      if (j + 1 < T && !fetch_and_send(j + 1)) { alive = false; break; }
+      // combine the tile max of the two halves of this row (bounded mbarrier meeting)
       __syncwarp();
       if (lane == 0) mbar_arrive(qbar);
       ok = wait_bar(qbar, j & 1, ctl, P.err, false);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
       mt = fmaxf(mt, rowmax[((j & 1) * 2 + (h ^ 1)) * ROWS + rr]);
+      if (tracer) MTV_TR(2, j, 3);
 
       const float m_new = fmaxf(m_ref, mt);
       const bool move = (m_new > m_ref + kRescaleLog2) || (m_ref == -INFINITY && m_new != -INFINITY);
       const float fac = move ? ex2(m_ref - m_new) : 1.f;  // ex2(-inf) = 0
+      if (move) {
+        l_bf *= fac;
+        l_true *= fac;
+        m_ref = m_new;
+      }
+      const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
+      float sb = 0.f, sbt = 0.f;
+      uint32_t pk[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const float p0 = ex2(x[2 * u] - mref), p1 = ex2(x[2 * u + 1] - mref);
+        const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
+        const float2 f = __bfloat1622float2(b);
+        sb += f.x + f.y;   // what the tensor core multiplies: normalises O
+        sbt += p0 + p1;    // unrounded weights: the LSE
+        pk[u] = *reinterpret_cast<const uint32_t*>(&b);
+      }
+      l_bf += sb;
+      l_true += sbt;
 
+      // GEMM2 of the previous tile must be done before O is rescaled and P reused
       if (j > 0) {
         ok = wait_bar(bar(B_O_READY), (j - 1) & 1, ctl, P.err, false);
         if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
         tc_fence_after();
+        if (tracer) MTV_TR(2, j, 4);
         if (__any_sync(0xffffffffu, move)) {  // warp-uniform TMEM read-modify-write of this warp's O half
 #pragma unroll 1
           for (int c0 = 128 * h; c0 < 128 * h + 128; c0 += 32) {
@@ -386,33 +462,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
           }
         }
       }
-      if (move) {
-        l_bf *= fac;
-        l_true *= fac;
-        m_ref = m_new;
-      }
-      const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sb = 0.f, st = 0.f;
-      uint32_t pk[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const float p0 = ex2(x[2 * u] - mref), p1 = ex2(x[2 * u + 1] - mref);
-        const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
-        const float2 f = __bfloat1622float2(b);
-        sb += f.x + f.y;   // what the tensor core multiplies: normalises O
-        st += p0 + p1;     // unrounded weights: the LSE
-        pk[u] = *reinterpret_cast<const uint32_t*>(&b);
-      }
-      l_bf += sb;
-      l_true += st;
-#pragma unroll
-      for (int u = 0; u < 4; ++u)
-        st_shared_v4(base + kOffP + uint32_t(rr) * 128u + ((uint32_t(4 * h + u) ^ uint32_t(rr & 7)) << 4),
-                     pk[4 * u], pk[4 * u + 1], pk[4 * u + 2], pk[4 * u + 3]);
-      fence_proxy_async_smem();
+      tmem_st16_sync(tmem + lane_off + kTmemP + 16 * h, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P_FULL));
+      if (tracer) MTV_TR(2, j, 5);
     }
 
     // epilogue: normalised O half (+ LSE from CTA 0)
@@ -528,3 +582,14 @@ cudaError_t launch_partial_tc(const Params& P, cudaStream_t st) {
 }
 
 }  // namespace mtv
+
+#ifdef MTV_TRACE
+extern "C" int mtv_trace_read(void* host, size_t bytes) {
+  if (bytes > sizeof(mtv::g_trace)) bytes = sizeof(mtv::g_trace);
+  return cudaMemcpyFromSymbol(host, mtv::g_trace, bytes) == cudaSuccess ? 0 : -7;
+}
+extern "C" int mtv_trace_clear() {
+  static long long zeros[4 * mtv::kTraceTiles * mtv::kTraceEvents];
+  return cudaMemcpyToSymbol(mtv::g_trace, zeros, sizeof(zeros)) == cudaSuccess ? 0 : -7;
+}
+#endif
