@@ -169,6 +169,38 @@ int mla_tree_verify_clear_device_error(void* workspace, void* stream);
  * diagnostics helper, not for use inside capture. */
 int mla_tree_verify_read_device_error(const void* workspace, uint32_t* flags_out, void* stream);
 
+/*
+ * mla_tree_verify_run_static -- the same pass as mla_tree_verify_run, for
+ * callers that cannot allocate device memory where they call attention: a
+ * step being recorded into a CUDA graph (allocation calls are not allowed
+ * while a stream captures), a host framework that owns every device
+ * allocation through its own pool, or a latency-critical path that must not
+ * touch an allocator.  The caller still owns and passes every input and
+ * output; only the workspace is replaced by a fixed device array inside this
+ * library.  (No counterpart on the pages: it is a packaging variant.)
+ *
+ * Limits and behaviour:
+ *   - the array holds 64 MiB on every GPU that loads the library, until the
+ *     process exits; a plan whose ws_bytes exceeds it is rejected with
+ *     MTV_E_WORKSPACE_SMALL (plan with nsplit_override = 1 to need only the
+ *     256-byte header);
+ *   - the first call on each device looks up the array's device address with
+ *     that device current: make that first call before any stream capture;
+ *   - every call shares the one array and it keeps the last call's contents;
+ *     calls whose kernels overlap on the GPU (other streams, other threads)
+ *     race on it, so serialise them;
+ *   - the device error word is cleared (an asynchronous 4-byte memset on
+ *     `stream`) at the start of each call; it is not reported back by this
+ *     entry point;
+ *   - no cudaMalloc, cudaFree or other allocating call is made.
+ * Arguments are those of mla_tree_verify_run without the workspace.
+ */
+int mla_tree_verify_run_static(const mtv_plan_t* plan, const void* q, const void* kv_pool,
+                               int64_t num_slots, const int64_t* kv_indices, const int32_t* kv_indptr,
+                               const int64_t* out_cache_loc, const int64_t* qo_indptr,
+                               const uint8_t* custom_mask, const int64_t* mask_indptr, float scale,
+                               void* out, float* lse, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -50,7 +50,8 @@ class MtvError(RuntimeError):
 
 _lib = None
 SYMBOLS = ("mla_tree_verify_plan", "mla_tree_verify_run", "mla_tree_verify_strerror",
-           "mla_tree_verify_clear_device_error", "mla_tree_verify_read_device_error")
+           "mla_tree_verify_clear_device_error", "mla_tree_verify_read_device_error",
+           "mla_tree_verify_run_static")
 
 
 def library_path() -> str:
@@ -79,6 +80,9 @@ def load(path: str | None = None):
     lib.mla_tree_verify_clear_device_error.restype = I32
     lib.mla_tree_verify_read_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     lib.mla_tree_verify_read_device_error.restype = I32
+    lib.mla_tree_verify_run_static.argtypes = [ctypes.POINTER(MtvPlan), P, P, I64, P, P, P, P, P, P,
+                                               ctypes.c_float, P, P, P]
+    lib.mla_tree_verify_run_static.restype = I32
     if path == library_path():
         _lib = lib
     return lib
@@ -142,6 +146,24 @@ def run(p: MtvPlan, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr,
         wsp, int(ws_bytes), _stream_handle(stream))
     if check and rc != MTV_OK:
         raise MtvError(rc, "mla_tree_verify_run")
+    return rc
+
+
+def run_static(p: MtvPlan, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr, custom_mask,
+               mask_indptr, scale: float, out, lse, stream=None, check: bool = True) -> int:
+    """The allocation-free entry point: like ``run`` without a workspace (the
+    library's fixed device scratch is used; see the header for its limits)."""
+    num_slots = kv_pool.shape[0] if isinstance(kv_pool, torch.Tensor) else 0
+    anyp = _ptr(out, torch.bfloat16, "out")
+    rc = load().mla_tree_verify_run_static(
+        ctypes.byref(p), _ptr(q, torch.bfloat16, "q", anyp), _ptr(kv_pool, torch.bfloat16, "kv_pool", anyp),
+        int(num_slots), _ptr(kv_indices, torch.int64, "kv_indices", anyp),
+        _ptr(kv_indptr, torch.int32, "kv_indptr"), _ptr(out_cache_loc, torch.int64, "out_cache_loc", anyp),
+        _ptr(qo_indptr, torch.int64, "qo_indptr"), _ptr(custom_mask, torch.uint8, "custom_mask", anyp),
+        _ptr(mask_indptr, torch.int64, "mask_indptr"), float(scale), anyp,
+        _ptr(lse, torch.float32, "lse"), _stream_handle(stream))
+    if check and rc != MTV_OK:
+        raise MtvError(rc, "mla_tree_verify_run_static")
     return rc
 
 
