@@ -18,25 +18,26 @@
 //      barrier, so the warps never wait for memory.  (Scattered 1152-byte
 //      rows: per-warp cp.async scales with the number of issuing warps, while
 //      TMA gathers are limited to about one 128-byte row per 18 cycles per SM);
-//   2. GEMM1 on the tensor core: S_c[128 x 64] = Q_c (TMEM, A operand) .
-//      K_c^T (smem), 18 k-steps of 16, fp32 accumulate in TMEM;
+//   2. GEMM1 on the tensor core: S_c[128 x 64] = Q_c . K_c^T, fp32 in TMEM;
+//      the latent part of Q_c is the A operand in TMEM (16 k-steps), its rope
+//      part an A operand in shared memory (2 k-steps);
 //   3. the softmax warps send their partial S to the peer CTA with st.async
 //      (completing bytes on the peer's barrier, double-buffered, one tile
 //      ahead), add the peer's partial (S_0 + S_1 is bit-identical on both
 //      CTAs), apply the tree mask (prefix always visible, tree columns from
 //      custom_mask), and run the fp32 online softmax ("Design Decisions and
 //      Trade-Offs": mask -> -inf, streaming max/sum) with a lazily moved
-//      reference max; P (bf16) goes to TMEM;
+//      reference max; P (bf16) goes to one of two TMEM buffers;
 //   4. GEMM2: O_c[128 x 256] += P (TMEM, A operand) . V_c, where V_c is this
 //      CTA's 256 latent dims of the same smem tile read as an MN-major operand.
 // Both CTAs take identical softmax decisions, so O_0 and O_1 are the two
 // halves of one consistent output.  The end of a split writes the normalised
 // partial O and its LSE (or the final bf16 output when there is one split).
 //
-// TMEM (512 columns): O half [0,256), partial S [256,320), Q half [320,464),
-// P [464,496).  Every wait is bounded: a timeout sets MTV_DEVERR_TIMEOUT and
-// the CTA winds down (its MMAs and copies drain, TMEM is freed) instead of
-// hanging.
+// TMEM (512 columns): O half [0,256), partial S [256,320), latent Q half
+// [320,448), P double buffer [448,512).  Every wait is bounded: a timeout sets
+// MTV_DEVERR_TIMEOUT and the CTA winds down (its MMAs and copies drain, TMEM
+// is freed) instead of hanging.
 //
 // Building with -DMTV_TRACE records clock64() timestamps of the pipeline
 // events of the first CTA into a device buffer (read with mtv_trace_read).
@@ -60,10 +61,10 @@ constexpr int STAGES = 4;   // gather pipeline depth
 constexpr int NPROD_WARPS = 7;
 constexpr int NSOFT_WARPS = 8;  // two per TMEM lane quarter, 32 key columns each
 constexpr int NTHREADS = 32 * (1 + NPROD_WARPS + NSOFT_WARPS);  // warp 0 MMA, 1-7 gather, 8-15 softmax
-constexpr int KSTEPS1 = (256 + 32) / 16;  // 18
 constexpr int KSTEPS2 = NK / 16;          // 4
 constexpr float kRescaleLog2 = 8.0f;      // move the reference max only past 2^8 growth
 constexpr long long kTimeoutCycles = 1ll << 31;
+constexpr int kMaxKeysPerGatherWarp = (NK + NPROD_WARPS - 1) / NPROD_WARPS;  // 10
 
 constexpr uint32_t kChunkBytes = NK * 128;                       // 64 latent dims x 64 keys
 constexpr uint32_t kRopeBytes = NK * 64;                          // 32 rope dims x 64 keys
@@ -71,24 +72,27 @@ constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;    // 36 KB
 constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffSx = kOffStages + STAGES * kStageBytes;   // peer's partial S, 2 buffers
 constexpr uint32_t kSxBytes = ROWS * NK * 4;
-constexpr uint32_t kOffVmask = kOffSx + 2 * kSxBytes;             // key validity bit masks
-constexpr uint32_t kVmaskBytes = STAGES * 8 * 8;  // [stage][gather warp] partial masks
+constexpr uint32_t kOffQRope = kOffSx + 2 * kSxBytes;             // rope part of Q, 64B-swizzled
+constexpr uint32_t kQRopeBytes = ROWS * 64;
+constexpr uint32_t kOffVmask = kOffQRope + kQRopeBytes;           // [stage][8] key validity masks
+constexpr uint32_t kVmaskBytes = STAGES * 8 * 8;
 constexpr uint32_t kOffRowMax = kOffVmask + kVmaskBytes;          // [2 tiles][2 halves][128 rows] f32
 constexpr uint32_t kRowMaxBytes = 2 * 2 * ROWS * 4;
-constexpr uint32_t kOffLsum = kOffRowMax + kRowMaxBytes;          // [2 sums][128 rows] f32
-constexpr uint32_t kLsumBytes = 2 * ROWS * 4;
+constexpr uint32_t kOffLsum = kOffRowMax + kRowMaxBytes;          // [128 rows] f32
+constexpr uint32_t kLsumBytes = ROWS * 4;
 constexpr uint32_t kOffBars = kOffLsum + kLsumBytes;
 constexpr uint32_t kOffCtl = kOffBars + 256;
 constexpr uint32_t kSmemBytes = kOffCtl + 64 + 1024;  // + slack for 1 KB alignment
 
-constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 320, kTmemP = 464;
+constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 320, kTmemP = 448;
 
 enum : int {
-  B_KV_FULL = 0, B_KV_EMPTY = STAGES, B_S_FULL = 2 * STAGES, B_S_FREE, B_P_FULL, B_O_READY, B_Q_READY,
-  B_SX_FULL0, B_SX_FULL1, B_FIN, B_QMAX, B_COUNT = B_QMAX + 4
+  B_KV_FULL = 0, B_KV_EMPTY = STAGES, B_S_FULL = 2 * STAGES, B_S_FREE, B_P_FULL0, B_P_FULL1, B_O_READY0,
+  B_O_READY1, B_Q_READY, B_SX_FULL0, B_SX_FULL1, B_FIN, B_QMAX, B_COUNT = B_QMAX + 4
 };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
+static_assert(kOffQRope % 1024 == 0, "64B-swizzled operand alignment");
 
 struct Ctl {
   uint32_t tmem_base;
@@ -159,8 +163,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     }
     mbar_init(bar(B_S_FULL), 1);
     mbar_init(bar(B_S_FREE), NSOFT_WARPS);
-    mbar_init(bar(B_P_FULL), NSOFT_WARPS);
-    mbar_init(bar(B_O_READY), 1);
+    mbar_init(bar(B_P_FULL0), NSOFT_WARPS);
+    mbar_init(bar(B_P_FULL1), NSOFT_WARPS);
+    mbar_init(bar(B_O_READY0), 1);
+    mbar_init(bar(B_O_READY1), 1);
     mbar_init(bar(B_Q_READY), NSOFT_WARPS);
     mbar_init(bar(B_SX_FULL0), 1);  // one local expect_tx arrival + the peer's st.async bytes
     mbar_init(bar(B_SX_FULL1), 1);
@@ -184,17 +190,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     if (lane == 0) {
       const uint32_t id1 = idesc_bf16_f32(128, NK, 0, 0);
       const uint32_t id2 = idesc_bf16_f32(128, 256, 0, 1);
+      // GEMM2 of tile jj: P from TMEM buffer jj&1, V from the tile's stage.
       auto gemm2 = [&](int jj) -> bool {
-        if (!wait_bar(bar(B_P_FULL), jj & 1, ctl, P.err, false)) return false;
+        if (!wait_bar(bar(B_P_FULL0 + (jj & 1)), (jj >> 1) & 1, ctl, P.err, false)) return false;
         MTV_TR(0, jj, 2);
         tc_fence_after();
         const uint32_t st = base + kOffStages + uint32_t(jj % STAGES) * kStageBytes;
+        const uint32_t pa = tmem + kTmemP + 32u * uint32_t(jj & 1);
 #pragma unroll
         for (int kk = 0; kk < KSTEPS2; ++kk) {
           const uint64_t bd = smem_desc(st + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
-          mma_ts(tmem + kTmemO, tmem + kTmemP + kk * 8, bd, id2, (jj > 0 || kk > 0) ? 1u : 0u);
+          mma_ts(tmem + kTmemO, pa + kk * 8, bd, id2, (jj > 0 || kk > 0) ? 1u : 0u);
         }
-        mma_commit(bar(B_O_READY));
+        mma_commit(bar(B_O_READY0 + (jj & 1)));
         mma_commit(bar(B_KV_EMPTY + jj % STAGES));
         return true;
       };
@@ -213,10 +221,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         tc_fence_after();
         const uint32_t st = base + kOffStages + uint32_t(s) * kStageBytes;
 #pragma unroll
-        for (int kk = 0; kk < KSTEPS1; ++kk) {
-          const uint64_t bd = kk < 16 ? smem_desc(st + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024, kSwizzle128B)
-                                      : smem_desc(st + 4 * kChunkBytes + (kk - 16) * 32, 16, 512, kSwizzle64B);
+        for (int kk = 0; kk < 16; ++kk) {
+          const uint64_t bd = smem_desc(st + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024, kSwizzle128B);
           mma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int kk = 0; kk < 2; ++kk) {
+          const uint64_t ad = smem_desc(base + kOffQRope + kk * 32, 16, 512, kSwizzle64B);
+          const uint64_t bd = smem_desc(st + 4 * kChunkBytes + kk * 32, 16, 512, kSwizzle64B);
+          mma_ss(tmem + kTmemS, ad, bd, id1, 1u);
         }
         mma_commit(bar(B_S_FULL));
         if (j >= 2) ok = gemm2(j - 2);
@@ -238,6 +251,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     // barrier when its own copies land: the warp only waits for a free stage.
     const int pw = warp - 1;
     const int nmine = (NK - pw + NPROD_WARPS - 1) / NPROD_WARPS;  // 10 or 9
+    // per-key swizzled destination offsets within a stage (same for every tile)
+    uint32_t lat_off[kMaxKeysPerGatherWarp], rope_off[kMaxKeysPerGatherWarp];
+#pragma unroll
+    for (int i = 0; i < kMaxKeysPerGatherWarp; ++i) {
+      const int kk = pw + NPROD_WARPS * i;
+      lat_off[i] = uint32_t(lane >> 3) * kChunkBytes + kk * 128 + (((lane & 7) ^ (kk & 7)) << 4);
+      rope_off[i] = 4 * kChunkBytes + kk * 64 + (((lane & 3) ^ ((kk >> 1) & 3)) << 4);
+    }
+    const unsigned char* pool_lat = reinterpret_cast<const unsigned char*>(P.kv_pool) + crank * 512 + lane * 16;
+    const unsigned char* pool_rope =
+        reinterpret_cast<const unsigned char*>(P.kv_pool) + 1024 + crank * 64 + (lane & 3) * 16;
     auto raw_slot = [&](int j) -> int64_t {
       int64_t v = -1;
       if (lane < nmine && j < T) {
@@ -249,11 +273,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     int64_t v0 = raw_slot(0), v1 = raw_slot(1);
     for (int j = 0; j < T; ++j) {
       const int s = j % STAGES;
-      int64_t slot = -1;  // checked slot of this lane's key
+      int slot = -1;  // checked slot of this lane's key (< 2^31 by the ABI contract)
       {
         const int64_t k = k_begin + int64_t(j) * NK + pw + NPROD_WARPS * lane;
         if (lane < nmine && k < k_end) {
-          if (v0 >= 0 && v0 < P.num_slots) slot = v0;
+          if (v0 >= 0 && v0 < P.num_slots) slot = int(v0);
           else atomicOr(P.err, MTV_DEVERR_SLOT_RANGE);
         }
       }
@@ -273,17 +297,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         vmask_all[s * 8 + pw] = (uint64_t(vhi) << 32) | vlo;
         mbar_arrive(fb);  // release: publishes this warp's mask
       }
-#pragma unroll 2
-      for (int i = 0; i < nmine; ++i) {
-        const int kk = pw + NPROD_WARPS * i;
-        const int64_t sl = __shfl_sync(0xffffffffu, slot, i);
-        const uint32_t lat = st + uint32_t(lane >> 3) * kChunkBytes + kk * 128 + (((lane & 7) ^ (kk & 7)) << 4);
-        const uint32_t rope = st + 4 * kChunkBytes + kk * 64 + (((lane & 3) ^ ((kk >> 1) & 3)) << 4);
-        const unsigned char* src = sl >= 0 ? reinterpret_cast<const unsigned char*>(P.kv_pool + sl * kDQK)
-                                           : reinterpret_cast<const unsigned char*>(P.q);
-        const uint32_t nbytes = sl >= 0 ? 16u : 0u;
-        cp_async_16_zfill(lat, src + (sl >= 0 ? crank * 512 + lane * 16 : 0), nbytes);
-        if (lane < 4) cp_async_16_zfill(rope, src + (sl >= 0 ? 1024 + crank * 64 + lane * 16 : 0), nbytes);
+#pragma unroll
+      for (int i = 0; i < kMaxKeysPerGatherWarp; ++i) {
+        if (i < nmine) {
+          const int sl = __shfl_sync(0xffffffffu, slot, i);
+          const int64_t row = int64_t(sl < 0 ? 0 : sl) * (kDQK * 2);
+          const uint32_t nbytes = sl >= 0 ? 16u : 0u;
+          cp_async_16_zfill(st + lat_off[i], pool_lat + row, nbytes);
+          if (lane < 4) cp_async_16_zfill(st + rope_off[i], pool_rope + row, nbytes);
+        }
       }
       cp_async_arrive_noinc(fb);
       if (pw == 0 && lane == 0) MTV_TR(1, j, 1);
@@ -302,29 +324,43 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     const int64_t out_row = R.q_off * kHeads + grow;  // (token, head) row of q/out/lse
     const uint32_t qbar = bar(B_QMAX + q);            // meeting point of the two warps of this quarter
     float* rowmax = reinterpret_cast<float*>(gbase + kOffRowMax);  // [tile&1][half][row]
-    float* lsum_s = reinterpret_cast<float*>(gbase + kOffLsum);    // [2][row]
+    float* lsum_s = reinterpret_cast<float*>(gbase + kOffLsum);    // [row]
     const bool tracer = (sw == 0 && lane == 0);
+    // Scores stay in raw (unscaled) units; the scale enters once per element in
+    // the exponent: p = 2^(x*c - m*c) with c = scale*log2(e).
+    const float c = P.scale_log2;
+    const float thr_raw = kRescaleLog2 / c;
 
-    // Q half -> TMEM (A operand of GEMM1): column c packs dims (2c, 2c+1); the
-    // two warps of a quarter take alternate 16-column chunks.
+    // Q half: latent dims -> TMEM (A operand, column j packs dims 2j, 2j+1; the
+    // two warps of a quarter take alternate 16-column chunks); rope dims ->
+    // shared memory in the 64B-swizzled K-major layout (half 0 writes them).
     {
       const __nv_bfloat16* qrow = P.q + out_row * kDQK;
 #pragma unroll 1
-      for (int c0 = 16 * h; c0 < 144; c0 += 32) {
+      for (int c0 = 16 * h; c0 < 128; c0 += 32) {
         uint32_t v[16];
         if (valid) {
-          const uint4* src = c0 < 128 ? reinterpret_cast<const uint4*>(qrow + crank * 256 + 2 * c0)
-                                      : reinterpret_cast<const uint4*>(qrow + 512 + crank * 32 + 2 * (c0 - 128));
+          const uint4* src = reinterpret_cast<const uint4*>(qrow + crank * 256 + 2 * c0);
 #pragma unroll
           for (int u = 0; u < 4; ++u) {
-            const uint4 x = __ldg(src + u);
-            v[4 * u] = x.x; v[4 * u + 1] = x.y; v[4 * u + 2] = x.z; v[4 * u + 3] = x.w;
+            const uint4 xq = __ldg(src + u);
+            v[4 * u] = xq.x; v[4 * u + 1] = xq.y; v[4 * u + 2] = xq.z; v[4 * u + 3] = xq.w;
           }
         } else {
 #pragma unroll
           for (int u = 0; u < 16; ++u) v[u] = 0u;
         }
         tmem_st16_sync(tmem + lane_off + kTmemQ + c0, v);
+      }
+      if (h == 0) {
+        const uint4* src = reinterpret_cast<const uint4*>(qrow + 512 + crank * 32);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 xq = valid ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+          st_shared_v4(base + kOffQRope + uint32_t(rr) * 64u + ((uint32_t(u) ^ ((uint32_t(rr) >> 1) & 3u)) << 4),
+                       xq.x, xq.y, xq.z, xq.w);
+        }
+        fence_proxy_async_smem();  // read by the tensor core through the async proxy
       }
       tc_fence_before();
       __syncwarp();
@@ -338,7 +374,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     // tile j after that read), so buffer (j+1)&1 is always free when written.
     const uint32_t sx_peer = mapa(base + kOffSx, peer) + uint32_t(rr) * 256u;
     const uint32_t peer_sx_full = mapa(bar(B_SX_FULL0), peer);  // + 8 for buffer 1
-    float m_ref = -INFINITY, l_bf = 0.f, l_true = 0.f;
+    float m_ref = -INFINITY, l = 0.f;
     bool alive = true;
     uint32_t s[32];  // this CTA's partial scores of the tile being finished
 
@@ -370,45 +406,45 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       bool ok = wait_bar(bar(B_SX_FULL0 + (j & 1)), (j >> 1) & 1, ctl, P.err, false);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
       if (tracer) MTV_TR(2, j, 2);
-      float x[32];
+      uint64_t x2[16];  // full scores of this warp's 32 columns, packed pairs
       {
-        const float4* sx_mine = reinterpret_cast<const float4*>(gbase + kOffSx + (j & 1) * kSxBytes + rr * 256);
+        const ulonglong2* sx_mine =
+            reinterpret_cast<const ulonglong2*>(gbase + kOffSx + (j & 1) * kSxBytes + rr * 256);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
-          const float4 v = sx_mine[(8 * h + u) ^ (rr & 15)];
-          x[4 * u] = __uint_as_float(s[4 * u]) + v.x;
-          x[4 * u + 1] = __uint_as_float(s[4 * u + 1]) + v.y;
-          x[4 * u + 2] = __uint_as_float(s[4 * u + 2]) + v.z;
-          x[4 * u + 3] = __uint_as_float(s[4 * u + 3]) + v.w;
+          const ulonglong2 v = sx_mine[(8 * h + u) ^ (rr & 15)];
+          x2[2 * u] = f2_add(uint64_t(s[4 * u]) | (uint64_t(s[4 * u + 1]) << 32), v.x);
+          x2[2 * u + 1] = f2_add(uint64_t(s[4 * u + 2]) | (uint64_t(s[4 * u + 3]) << 32), v.y);
         }
       }
+      float x[32];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) f2_unpack(x2[u], x[2 * u], x[2 * u + 1]);
 
-      // mask + scale (log2 domain)
+      // tree mask (raw units; masked -> -inf)
       const int sidx = j % STAGES;
       ok = wait_bar(bar(B_KV_FULL + sidx), (j / STAGES) & 1, ctl, P.err, false);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
-      uint64_t vm = 0;
-#pragma unroll
-      for (int w = 0; w < NPROD_WARPS; ++w) vm |= vmask_all[sidx * 8 + w];
+      uint64_t vm;
+      {
+        const ulonglong2* vp = reinterpret_cast<const ulonglong2*>(vmask_all + sidx * 8);
+        const ulonglong2 a = vp[0], b = vp[1], cc = vp[2], d = vp[3];
+        vm = a.x | a.y | b.x | b.y | cc.x | cc.y | d.x;
+      }
       const uint32_t vbits = uint32_t(vm >> (32 * h));
       const int64_t kt = k_begin + int64_t(j) * NK + 32 * h;  // key of this warp's first column
-      float mt = -INFINITY;
-      if (valid && vbits == 0xffffffffu && kt + 32 <= R.p) {  // all prefix keys, all resolved
+      if (!(valid && vbits == 0xffffffffu && kt + 32 <= R.p)) {  // not an all-prefix, all-valid tile
 #pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          x[c] *= P.scale_log2;
-          mt = fmaxf(mt, x[c]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int64_t k = kt + c;
-          bool vis = valid && ((vbits >> c) & 1u);
+        for (int cc = 0; cc < 32; ++cc) {
+          const int64_t k = kt + cc;
+          bool vis = valid && ((vbits >> cc) & 1u);
           if (vis && k >= R.p) vis = tree_visible(P, R, ti, k - R.p);
-          x[c] = vis ? x[c] * P.scale_log2 : -INFINITY;
-          mt = fmaxf(mt, x[c]);
+          if (!vis) x[cc] = -INFINITY;
         }
       }
+      float mt = -INFINITY;
+#pragma unroll
+      for (int cc = 0; cc < 32; cc += 2) mt = max3(mt, x[cc], x[cc + 1]);
       // The tile max depends on every value read from the exchange buffer, so
       // once it is stored those reads are complete and tile j+1 may be sent
       // (the peer writes our buffer j&1 again only after receiving it).
@@ -423,83 +459,84 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       if (tracer) MTV_TR(2, j, 3);
 
       const float m_new = fmaxf(m_ref, mt);
-      const bool move = (m_new > m_ref + kRescaleLog2) || (m_ref == -INFINITY && m_new != -INFINITY);
-      const float fac = move ? ex2(m_ref - m_new) : 1.f;  // ex2(-inf) = 0
+      const bool move = (m_new > m_ref + thr_raw) || (m_ref == -INFINITY && m_new != -INFINITY);
+      const float fac = move ? ex2((m_ref - m_new) * c) : 1.f;  // ex2(-inf) = 0
       if (move) {
-        l_bf *= fac;
-        l_true *= fac;
+        l *= fac;
         m_ref = m_new;
       }
-      const float mref = (m_ref == -INFINITY) ? 0.f : m_ref;
-      float sb = 0.f, sbt = 0.f;
+      const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
+      const uint64_t c2 = f2_pack(c, c), nb2 = f2_pack(nb, nb);
+      uint64_t lsum2 = f2_pack(0.f, 0.f);
       uint32_t pk[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
-        const float p0 = ex2(x[2 * u] - mref), p1 = ex2(x[2 * u + 1] - mref);
+        float e0, e1;
+        f2_unpack(f2_fma(f2_pack(x[2 * u], x[2 * u + 1]), c2, nb2), e0, e1);
+        const float p0 = ex2(e0), p1 = ex2(e1);
+        lsum2 = f2_add(lsum2, f2_pack(p0, p1));
         const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
-        const float2 f = __bfloat1622float2(b);
-        sb += f.x + f.y;   // what the tensor core multiplies: normalises O
-        sbt += p0 + p1;    // unrounded weights: the LSE
         pk[u] = *reinterpret_cast<const uint32_t*>(&b);
       }
-      l_bf += sb;
-      l_true += sbt;
+      {
+        float a0, a1;
+        f2_unpack(lsum2, a0, a1);
+        l += a0 + a1;  // unrounded weights normalise O and give the LSE
+      }
 
-      // GEMM2 of the previous tile must be done before O is rescaled and P reused
-      if (j > 0) {
-        ok = wait_bar(bar(B_O_READY), (j - 1) & 1, ctl, P.err, false);
+      // P buffer j&1 was last read by GEMM2(j-2); O may only be rescaled once
+      // GEMM2(j-1) has finished accumulating into it.
+      if (j >= 2) {
+        ok = wait_bar(bar(B_O_READY0 + (j & 1)), ((j - 2) >> 1) & 1, ctl, P.err, false);
+        if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+      }
+      if (j >= 1 && __any_sync(0xffffffffu, move)) {  // warp-uniform TMEM read-modify-write of this warp's O half
+        ok = wait_bar(bar(B_O_READY0 + ((j - 1) & 1)), ((j - 1) >> 1) & 1, ctl, P.err, false);
         if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
         tc_fence_after();
-        if (tracer) MTV_TR(2, j, 4);
-        if (__any_sync(0xffffffffu, move)) {  // warp-uniform TMEM read-modify-write of this warp's O half
 #pragma unroll 1
-          for (int c0 = 128 * h; c0 < 128 * h + 128; c0 += 32) {
-            uint32_t v[32];
-            tmem_ld32_sync(tmem + lane_off + kTmemO + c0, v);
+        for (int c0 = 128 * h; c0 < 128 * h + 128; c0 += 32) {
+          uint32_t v[32];
+          tmem_ld32_sync(tmem + lane_off + kTmemO + c0, v);
 #pragma unroll
-            for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * fac);
-            tmem_st32_sync(tmem + lane_off + kTmemO + c0, v);
-          }
+          for (int u = 0; u < 32; ++u) v[u] = __float_as_uint(__uint_as_float(v[u]) * fac);
+          tmem_st32_sync(tmem + lane_off + kTmemO + c0, v);
         }
       }
-      tmem_st16_sync(tmem + lane_off + kTmemP + 16 * h, pk);
+      tc_fence_after();
+      if (tracer) MTV_TR(2, j, 4);
+      tmem_st16_sync(tmem + lane_off + kTmemP + 32 * (j & 1) + 16 * h, pk);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(B_P_FULL));
+      if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (j & 1)));
       if (tracer) MTV_TR(2, j, 5);
     }
 
     // epilogue: normalised O half (+ LSE from CTA 0)
     if (alive) {
-      bool ok = wait_bar(bar(B_O_READY), (T - 1) & 1, ctl, P.err, false);
+      bool ok = wait_bar(bar(B_O_READY0 + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl, P.err, false);
       alive = __all_sync(0xffffffffu, ok);
     }
     // the row's two partial sums (one per half) meet in shared memory: half 1
-    // publishes, half 0 adds and publishes the totals, half 1 reads them back
+    // publishes, half 0 adds, both read the total
     if (alive) {
-      if (h == 1) {
-        lsum_s[rr] = l_bf;
-        lsum_s[ROWS + rr] = l_true;
-      }
+      if (h == 1) lsum_s[rr] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(qbar);
       bool ok = wait_bar(qbar, T & 1, ctl, P.err, false);
       alive = __all_sync(0xffffffffu, ok);
     }
     if (alive) {
-      if (h == 0) {
-        lsum_s[rr] += l_bf;
-        lsum_s[ROWS + rr] += l_true;
-      }
+      if (h == 0) lsum_s[rr] += l;
       __syncwarp();
       if (lane == 0) mbar_arrive(qbar);
       bool ok = wait_bar(qbar, (T + 1) & 1, ctl, P.err, false);
       alive = __all_sync(0xffffffffu, ok);
     }
     if (alive) {
-      const float tot_bf = lsum_s[rr], tot_true = lsum_s[ROWS + rr];
+      const float tot = lsum_s[rr];
       tc_fence_after();
-      const float inv = tot_bf > 0.f ? 1.f / tot_bf : 0.f;
+      const float inv = tot > 0.f ? 1.f / tot : 0.f;
 #pragma unroll 1
       for (int c0 = 128 * h; c0 < 128 * h + 128; c0 += 32) {
         uint32_t v[32];
@@ -529,7 +566,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         }
       }
       if (valid && crank == 0 && h == 0) {
-        const float lse = tot_true > 0.f ? (m_ref + __log2f(tot_true)) * kLn2 : -INFINITY;
+        const float lse = tot > 0.f ? (m_ref * c + __log2f(tot)) * kLn2 : -INFINITY;
         if (P.nsplit == 1) P.lse[out_row] = lse;
         else P.part_lse[int64_t(split) * P.total_q_max * kHeads + out_row] = lse;
       }
