@@ -23,16 +23,20 @@
 //      part an A operand in shared memory (2 k-steps);
 //   3. the softmax warps send their partial S to the peer CTA with st.async
 //      (completing bytes on the peer's barrier, double-buffered, one tile
-//      ahead), add the peer's partial (S_0 + S_1 is bit-identical on both
-//      CTAs), apply the tree mask (prefix always visible, tree columns from
+//      ahead) as 16-bit integers with one power-of-two exponent per 32 values
+//      (block floating point: error <= 2^-15 of the block's largest
+//      magnitude; the distributed-shared-memory link, not the arithmetic, is
+//      what this exchange costs), add the peer's partial to their own exact
+//      one, apply the tree mask (prefix always visible, tree columns from
 //      custom_mask), and run the fp32 online softmax ("Design Decisions and
 //      Trade-Offs": mask -> -inf, streaming max/sum) with a lazily moved
-//      reference max; P (bf16) goes to one of two TMEM buffers;
+//      reference max; P (bf16) goes to one of two TMEM buffers.  Each CTA
+//      normalises its own O half with its own softmax sums, so the two views
+//      of S need not be bit-identical;
 //   4. GEMM2: O_c[128 x 256] += P (TMEM, A operand) . V_c, where V_c is this
 //      CTA's 256 latent dims of the same smem tile read as an MN-major operand.
-// Both CTAs take identical softmax decisions, so O_0 and O_1 are the two
-// halves of one consistent output.  The end of a split writes the normalised
-// partial O and its LSE (or the final bf16 output when there is one split).
+// The end of a split writes the normalised partial O halves and the LSE of
+// CTA 0 (or the final bf16 output when there is one split).
 //
 // TMEM (512 columns): O half [0,256), partial S [256,320), latent Q half
 // [320,448), P double buffer [448,512).  Every wait is bounded: a timeout sets
@@ -58,7 +62,7 @@ using namespace ptx;
 constexpr int ROWS = 128;   // query rows per CTA pair
 constexpr int NK = 64;      // keys per tile
 constexpr int STAGES = 4;   // gather pipeline depth
-constexpr int NPROD_WARPS = 7;
+constexpr int NPROD_WARPS = 4;
 constexpr int NSOFT_WARPS = 8;  // two per TMEM lane quarter, 32 key columns each
 constexpr int NTHREADS = 32 * (1 + NPROD_WARPS + NSOFT_WARPS);  // warp 0 MMA, 1-7 gather, 8-15 softmax
 constexpr int KSTEPS2 = NK / 16;          // 4
@@ -70,9 +74,12 @@ constexpr uint32_t kChunkBytes = NK * 128;                       // 64 latent di
 constexpr uint32_t kRopeBytes = NK * 64;                          // 32 rope dims x 64 keys
 constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;    // 36 KB
 constexpr uint32_t kOffStages = 0;
-constexpr uint32_t kOffSx = kOffStages + STAGES * kStageBytes;   // peer's partial S, 2 buffers
-constexpr uint32_t kSxBytes = ROWS * NK * 4;
-constexpr uint32_t kOffQRope = kOffSx + 2 * kSxBytes;             // rope part of Q, 64B-swizzled
+// Peer's partial S, 2 buffers of [half][row] x (32 x int16 = 64 B) + [half][row] exponents.
+constexpr uint32_t kOffSx = kOffStages + STAGES * kStageBytes;
+constexpr uint32_t kSxDataBytes = 2 * ROWS * 64;
+constexpr uint32_t kSxBytes = kSxDataBytes + 2 * ROWS * 4;        // bytes completed per tile: 17408
+constexpr uint32_t kSxStride = (kSxBytes + 1023) & ~1023u;
+constexpr uint32_t kOffQRope = kOffSx + 2 * kSxStride;            // rope part of Q, 64B-swizzled
 constexpr uint32_t kQRopeBytes = ROWS * 64;
 constexpr uint32_t kOffVmask = kOffQRope + kQRopeBytes;           // [stage][8] key validity masks
 constexpr uint32_t kVmaskBytes = STAGES * 8 * 8;
@@ -93,6 +100,7 @@ enum : int {
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kOffQRope % 1024 == 0, "64B-swizzled operand alignment");
+static_assert(NPROD_WARPS <= 8, "one 64-bit validity word per gather warp, 8 per stage");
 
 struct Ctl {
   uint32_t tmem_base;
@@ -367,18 +375,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       if (lane == 0) mbar_arrive(bar(B_Q_READY));
     }
 
-    // Partial-score exchange, double-buffered: the partial of tile j goes to
-    // the peer's buffer j&1 and completes bytes on its barrier SX_FULL(j&1).
+    // Partial-score exchange, double-buffered: the (quantised) partial of tile
+    // j goes to the peer's buffer j&1 and completes bytes on its barrier
+    // SX_FULL(j&1).
     // A CTA sends tile j+1 only after it has consumed tile j, and it consumed
     // tile j only after the peer had finished reading tile j-1 (the peer sent
     // tile j after that read), so buffer (j+1)&1 is always free when written.
-    const uint32_t sx_peer = mapa(base + kOffSx, peer) + uint32_t(rr) * 256u;
+    const uint32_t sx_peer = mapa(base + kOffSx, peer);
     const uint32_t peer_sx_full = mapa(bar(B_SX_FULL0), peer);  // + 8 for buffer 1
     float m_ref = -INFINITY, l = 0.f;
     bool alive = true;
     uint32_t s[32];  // this CTA's partial scores of the tile being finished
 
-    // load tile jn's partial scores from TMEM and send them to the peer
+    // load tile jn's partial scores from TMEM and send them to the peer as
+    // 32 int16 with a shared exponent k: q = rint(v * 2^(14-k)), max|v| < 2^k
     auto fetch_and_send = [&](int jn) -> bool {
       bool ok = wait_bar(bar(B_S_FULL), jn & 1, ctl, P.err, false);
       if (!__all_sync(0xffffffffu, ok)) return false;
@@ -388,12 +398,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_S_FREE));
-      const uint32_t dst = sx_peer + uint32_t(jn & 1) * kSxBytes;
-      const uint32_t pbar = peer_sx_full + 8u * uint32_t(jn & 1);
+      float amax = 0.f;
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_async_v4(dst + ((uint32_t(8 * h + u) ^ uint32_t(rr & 15)) << 4), s[4 * u], s[4 * u + 1], s[4 * u + 2],
-                    s[4 * u + 3], pbar);
+      for (int u = 0; u < 32; u += 2)
+        amax = max3(amax, fabsf(__uint_as_float(s[u])), fabsf(__uint_as_float(s[u + 1])));
+      int k = 0;
+      frexpf(amax, &k);                  // amax < 2^k (0 -> k = 0)
+      k = max(-100, min(k, 100));
+      const float qs = __int_as_float((127 + 14 - k) << 23);  // 2^(14-k), exact
+      uint32_t w[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        const int a = __float2int_rn(__uint_as_float(s[2 * u]) * qs);
+        const int b = __float2int_rn(__uint_as_float(s[2 * u + 1]) * qs);
+        w[u] = (uint32_t(a) & 0xffffu) | (uint32_t(b) << 16);
+      }
+      const uint32_t buf = uint32_t(jn & 1) * kSxStride;
+      const uint32_t pbar = peer_sx_full + 8u * uint32_t(jn & 1);
+      const uint32_t drow = sx_peer + buf + uint32_t(h) * (ROWS * 64) + uint32_t(rr) * 64u;
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        st_async_v4(drow + ((uint32_t(u) ^ ((uint32_t(rr) >> 1) & 3u)) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2],
+                    w[4 * u + 3], pbar);
+      st_async_b32(sx_peer + buf + kSxDataBytes + uint32_t(h * ROWS + rr) * 4u, uint32_t(k), pbar);
       if (tracer) MTV_TR(2, jn, 1);
       return true;
     };
@@ -406,30 +433,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       bool ok = wait_bar(bar(B_SX_FULL0 + (j & 1)), (j >> 1) & 1, ctl, P.err, false);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
       if (tracer) MTV_TR(2, j, 2);
-      uint64_t x2[16];  // full scores of this warp's 32 columns, packed pairs
+      float x[32];  // full scores of this warp's 32 columns: own exact partial + peer's
       {
-        const ulonglong2* sx_mine =
-            reinterpret_cast<const ulonglong2*>(gbase + kOffSx + (j & 1) * kSxBytes + rr * 256);
+        const unsigned char* rxb = gbase + kOffSx + (j & 1) * kSxStride;
+        const int kp = *reinterpret_cast<const int*>(rxb + kSxDataBytes + (h * ROWS + rr) * 4);
+        const float dq = __int_as_float((127 - 14 + kp) << 23);  // 2^(k-14)
+        const uint4* row = reinterpret_cast<const uint4*>(rxb + h * (ROWS * 64) + rr * 64);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const ulonglong2 v = sx_mine[(8 * h + u) ^ (rr & 15)];
-          x2[2 * u] = f2_add(uint64_t(s[4 * u]) | (uint64_t(s[4 * u + 1]) << 32), v.x);
-          x2[2 * u + 1] = f2_add(uint64_t(s[4 * u + 2]) | (uint64_t(s[4 * u + 3]) << 32), v.y);
+        for (int u = 0; u < 4; ++u) {
+          const uint4 v = row[u ^ ((rr >> 1) & 3)];
+          const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int lo = int(wv[e] << 16) >> 16, hi = int(wv[e]) >> 16;
+            x[8 * u + 2 * e] = fmaf(float(lo), dq, __uint_as_float(s[8 * u + 2 * e]));
+            x[8 * u + 2 * e + 1] = fmaf(float(hi), dq, __uint_as_float(s[8 * u + 2 * e + 1]));
+          }
         }
       }
-      float x[32];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) f2_unpack(x2[u], x[2 * u], x[2 * u + 1]);
 
       // tree mask (raw units; masked -> -inf)
       const int sidx = j % STAGES;
       ok = wait_bar(bar(B_KV_FULL + sidx), (j / STAGES) & 1, ctl, P.err, false);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
-      uint64_t vm;
+      uint64_t vm = 0;  // OR of the gather warps' masks (exactly NPROD_WARPS words are written)
       {
         const ulonglong2* vp = reinterpret_cast<const ulonglong2*>(vmask_all + sidx * 8);
-        const ulonglong2 a = vp[0], b = vp[1], cc = vp[2], d = vp[3];
-        vm = a.x | a.y | b.x | b.y | cc.x | cc.y | d.x;
+#pragma unroll
+        for (int w2 = 0; w2 < NPROD_WARPS / 2; ++w2) {
+          const ulonglong2 a = vp[w2];
+          vm |= a.x | a.y;
+        }
+        if (NPROD_WARPS & 1) vm |= vmask_all[sidx * 8 + NPROD_WARPS - 1];
       }
       const uint32_t vbits = uint32_t(vm >> (32 * h));
       const int64_t kt = k_begin + int64_t(j) * NK + 32 * h;  // key of this warp's first column

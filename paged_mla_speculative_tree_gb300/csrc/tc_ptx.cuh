@@ -75,6 +75,11 @@ __device__ __forceinline__ void st_async_v4(uint32_t addr, uint32_t a, uint32_t 
                "r"(a), "r"(b), "r"(c), "r"(d), "r"(cluster_bar)
                : "memory");
 }
+__device__ __forceinline__ void st_async_b32(uint32_t addr, uint32_t a, uint32_t cluster_bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(addr), "r"(a),
+               "r"(cluster_bar)
+               : "memory");
+}
 __device__ __forceinline__ void st_cluster_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared::cluster.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
