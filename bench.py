@@ -337,17 +337,19 @@ def e2e_step(host, d, call, out, lse, out_h, lse_h):
 
 
 def load_traffic(workload_name, plan):
-    """DRAM bytes per call from the committed ncu summary, if it matches this build."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+    """DRAM bytes per launch of the partial kernel from the committed ncu
+    summary (profiles/traffic.md), if it was measured on these kernel sources."""
+    path = os.path.join(ROOT, "profiles", "traffic.md")
     if not os.path.exists(path):
         return None
-    try:
-        d = json.load(open(path))
-        e = d.get(workload_name)
-        if e and e.get("kernel_rev") == kernel_revision():
-            return e.get("dram_bytes_per_call")
-    except Exception:
-        return None
+    rev = kernel_revision()
+    for line in open(path):
+        cells = [c.strip() for c in line.strip().strip("|").split("|")]
+        if len(cells) == 3 and cells[0] == workload_name and cells[1] == rev:
+            try:
+                return int(cells[2])
+            except ValueError:
+                return None
     return None
 
 
