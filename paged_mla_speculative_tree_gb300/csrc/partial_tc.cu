@@ -11,7 +11,7 @@
 //
 // The 576 contraction dims are split between the two CTAs: CTA c holds latent
 // dims [256c, 256c+256) and rope dims [32c, 32c+32).  Per 64-key tile:
-//   1. seven gather warps copy the CTA's 576 bytes of each latent row with
+//   1. three gather warps copy the CTA's 576 bytes of each latent row with
 //      cp.async (16 B per lane, one row per warp instruction) into a
 //      128B-swizzled K-major tile (64B swizzle for the rope part); invalid
 //      slots are zero-filled; each lane's copies complete on the stage's
@@ -23,12 +23,13 @@
 //      part an A operand in shared memory (2 k-steps);
 //   3. the softmax warps send their partial S to the peer CTA with st.async
 //      (completing bytes on the peer's barrier, double-buffered, one tile
-//      ahead) as 16-bit integers with one power-of-two exponent per 32 values
+//      ahead) as 16-bit integers with one power-of-two exponent per 16 values
 //      (block floating point: error <= 2^-15 of the block's largest
 //      magnitude; the distributed-shared-memory link, not the arithmetic, is
 //      what this exchange costs), add the peer's partial to their own exact
 //      one, apply the tree mask (prefix always visible, tree columns from
-//      custom_mask), and run the fp32 online softmax ("Design Decisions and
+//      custom_mask), and run the fp32 online softmax (four warps per row
+//      quarter, 16 key columns each; "Design Decisions and
 //      Trade-Offs": mask -> -inf, streaming max/sum) with a lazily moved
 //      reference max; P (bf16) goes to one of two TMEM buffers.  Each CTA
 //      normalises its own O half with its own softmax sums, so the two views
@@ -62,31 +63,39 @@ using namespace ptx;
 constexpr int ROWS = 128;   // query rows per CTA pair
 constexpr int NK = 64;      // keys per tile
 constexpr int STAGES = 4;   // gather pipeline depth
-constexpr int NPROD_WARPS = 4;
-constexpr int NSOFT_WARPS = 8;  // two per TMEM lane quarter, 32 key columns each
-constexpr int NTHREADS = 32 * (1 + NPROD_WARPS + NSOFT_WARPS);  // warp 0 MMA, 1-7 gather, 8-15 softmax
+#ifndef MTV_TC_GATHER_WARPS
+#define MTV_TC_GATHER_WARPS 3  // 3 + 16 + 1 warps leave 96 registers per thread
+#endif
+constexpr int NPROD_WARPS = MTV_TC_GATHER_WARPS;
+constexpr int NSOFT_WARPS = 16;            // four per TMEM lane quarter
+constexpr int WPQ = NSOFT_WARPS / 4;       // softmax warps sharing one lane quarter (one row)
+constexpr int NCOL = NK / WPQ;             // key columns per softmax warp: 16
+constexpr int OCOLS = 256 / WPQ;           // O columns per softmax warp (rescale, epilogue): 64
+constexpr int XU = NCOL * 2 / 16;          // 16-byte units of one thread's quantised partial row: 2
+constexpr int NTHREADS = 32 * (1 + NPROD_WARPS + NSOFT_WARPS);  // warp 0 MMA, then gather, then softmax
 constexpr int KSTEPS2 = NK / 16;          // 4
 constexpr float kRescaleLog2 = 8.0f;      // move the reference max only past 2^8 growth
+constexpr float kQuantMagic = 12615680.0f;  // 1.5 * 2^23 + 2^15
 constexpr long long kTimeoutCycles = 1ll << 31;
-constexpr int kMaxKeysPerGatherWarp = (NK + NPROD_WARPS - 1) / NPROD_WARPS;  // 10
+constexpr int kMaxKeysPerGatherWarp = (NK + NPROD_WARPS - 1) / NPROD_WARPS;
 
 constexpr uint32_t kChunkBytes = NK * 128;                       // 64 latent dims x 64 keys
 constexpr uint32_t kRopeBytes = NK * 64;                          // 32 rope dims x 64 keys
 constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;    // 36 KB
 constexpr uint32_t kOffStages = 0;
-// Peer's partial S, 2 buffers of [half][row] x (32 x int16 = 64 B) + [half][row] exponents.
+// Peer's partial S, 2 buffers of [warp h][row] x (NCOL int16) + [warp h][row] exponents.
 constexpr uint32_t kOffSx = kOffStages + STAGES * kStageBytes;
-constexpr uint32_t kSxDataBytes = 2 * ROWS * 64;
-constexpr uint32_t kSxBytes = kSxDataBytes + 2 * ROWS * 4;        // bytes completed per tile: 17408
+constexpr uint32_t kSxDataBytes = WPQ * ROWS * NCOL * 2;
+constexpr uint32_t kSxBytes = kSxDataBytes + WPQ * ROWS * 4;      // bytes completed per tile
 constexpr uint32_t kSxStride = (kSxBytes + 1023) & ~1023u;
 constexpr uint32_t kOffQRope = kOffSx + 2 * kSxStride;            // rope part of Q, 64B-swizzled
 constexpr uint32_t kQRopeBytes = ROWS * 64;
 constexpr uint32_t kOffVmask = kOffQRope + kQRopeBytes;           // [stage][8] key validity masks
 constexpr uint32_t kVmaskBytes = STAGES * 8 * 8;
-constexpr uint32_t kOffRowMax = kOffVmask + kVmaskBytes;          // [2 tiles][2 halves][128 rows] f32
-constexpr uint32_t kRowMaxBytes = 2 * 2 * ROWS * 4;
-constexpr uint32_t kOffLsum = kOffRowMax + kRowMaxBytes;          // [128 rows] f32
-constexpr uint32_t kLsumBytes = ROWS * 4;
+constexpr uint32_t kOffRowMax = kOffVmask + kVmaskBytes;          // [2 tiles][WPQ][128 rows] f32
+constexpr uint32_t kRowMaxBytes = 2 * WPQ * ROWS * 4;
+constexpr uint32_t kOffLsum = kOffRowMax + kRowMaxBytes;          // [WPQ][128 rows] f32
+constexpr uint32_t kLsumBytes = WPQ * ROWS * 4;
 constexpr uint32_t kOffBars = kOffLsum + kLsumBytes;
 constexpr uint32_t kOffCtl = kOffBars + 256;
 constexpr uint32_t kSmemBytes = kOffCtl + 64 + 1024;  // + slack for 1 KB alignment
@@ -101,6 +110,7 @@ static_assert(B_COUNT * 8 <= 256, "barrier area");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kOffQRope % 1024 == 0, "64B-swizzled operand alignment");
 static_assert(NPROD_WARPS <= 8, "one 64-bit validity word per gather warp, 8 per stage");
+static_assert(NCOL % 8 == 0 && XU >= 1 && (XU & (XU - 1)) == 0, "softmax column split");
 
 struct Ctl {
   uint32_t tmem_base;
@@ -141,6 +151,11 @@ __device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl, u
   }
 }
 
+// Inline fast path: most waits find the phase already complete.
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, Ctl* ctl, unsigned* err) {
+  return mbar_try_wait(bar, parity) || wait_bar(bar, parity, ctl, err, false);
+}
+
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params P) {
   extern __shared__ unsigned char smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -179,7 +194,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     mbar_init(bar(B_SX_FULL0), 1);  // one local expect_tx arrival + the peer's st.async bytes
     mbar_init(bar(B_SX_FULL1), 1);
     mbar_init(bar(B_FIN), 1);
-    for (int qq = 0; qq < 4; ++qq) mbar_init(bar(B_QMAX + qq), 2);
+    for (int qq = 0; qq < 4; ++qq) mbar_init(bar(B_QMAX + qq), WPQ);
     ctl->abort = 0;
     fence_mbar_init_cluster();
   }
@@ -250,7 +265,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     __syncwarp();
   } else if (warp <= NPROD_WARPS) {
     // ------------------------------------------------------------ gather
-    // Warp pw copies keys pw, pw+7, ... of each tile (10 or 9 keys).  Lane i
+    // Warp pw copies keys pw, pw + NPROD_WARPS, ... of each tile.  Lane i
     // holds the slot of the warp's i-th key, loaded two tiles ahead and only
     // checked when used, so index latency never stalls the warp.  Per key the
     // warp issues one 512-byte latent copy (32 lanes x 16 B) and one 64-byte
@@ -258,7 +273,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     // zero-filled (source size 0).  Each lane then arrives on the stage's
     // barrier when its own copies land: the warp only waits for a free stage.
     const int pw = warp - 1;
-    const int nmine = (NK - pw + NPROD_WARPS - 1) / NPROD_WARPS;  // 10 or 9
+    const int nmine = (NK - pw + NPROD_WARPS - 1) / NPROD_WARPS;
     // per-key swizzled destination offsets within a stage (same for every tile)
     uint32_t lat_off[kMaxKeysPerGatherWarp], rope_off[kMaxKeysPerGatherWarp];
 #pragma unroll
@@ -321,18 +336,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     cp_async_wait<0>();  // no copy may be in flight when the CTA exits
   } else {
     // ------------------------------------------------------------ softmax / epilogue
-    const int sw = warp - 1 - NPROD_WARPS;         // 0..7
+    const int sw = warp - 1 - NPROD_WARPS;         // 0 .. NSOFT_WARPS-1
     const int q = warp & 3;                        // TMEM lane quarter this warp may access
-    const int h = sw >> 2;                         // key columns [32h, 32h+32), O columns [128h, +128)
+    const int h = sw >> 2;                         // key columns [NCOL*h, +NCOL), O columns [OCOLS*h, +OCOLS)
     const int rr = q * 32 + lane;                  // row within the pair tile = TMEM lane
     const int64_t grow = int64_t(rb) * ROWS + rr;  // row within the request
     const bool valid = grow < rows_req;
     const int64_t ti = grow / kHeads;              // tree token of this row
     const uint32_t lane_off = uint32_t(q * 32) << 16;
     const int64_t out_row = R.q_off * kHeads + grow;  // (token, head) row of q/out/lse
-    const uint32_t qbar = bar(B_QMAX + q);            // meeting point of the two warps of this quarter
-    float* rowmax = reinterpret_cast<float*>(gbase + kOffRowMax);  // [tile&1][half][row]
-    float* lsum_s = reinterpret_cast<float*>(gbase + kOffLsum);    // [row]
+    const uint32_t qbar = bar(B_QMAX + q);            // meeting point of the WPQ warps of this quarter
+    float* rowmax = reinterpret_cast<float*>(gbase + kOffRowMax);  // [tile&1][h][row]
+    float* lsum_s = reinterpret_cast<float*>(gbase + kOffLsum);    // [h][row]
     const bool tracer = (sw == 0 && lane == 0);
     // Scores stay in raw (unscaled) units; the scale enters once per element in
     // the exponent: p = 2^(x*c - m*c) with c = scale*log2(e).
@@ -340,12 +355,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     const float thr_raw = kRescaleLog2 / c;
 
     // Q half: latent dims -> TMEM (A operand, column j packs dims 2j, 2j+1; the
-    // two warps of a quarter take alternate 16-column chunks); rope dims ->
-    // shared memory in the 64B-swizzled K-major layout (half 0 writes them).
+    // warps of a quarter take 16-column chunks in turn); rope dims -> shared
+    // memory in the 64B-swizzled K-major layout (warp h = 0 writes them).
     {
       const __nv_bfloat16* qrow = P.q + out_row * kDQK;
 #pragma unroll 1
-      for (int c0 = 16 * h; c0 < 128; c0 += 32) {
+      for (int c0 = 16 * h; c0 < 128; c0 += 16 * WPQ) {
         uint32_t v[16];
         if (valid) {
           const uint4* src = reinterpret_cast<const uint4*>(qrow + crank * 256 + 2 * c0);
@@ -377,49 +392,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
 
     // Partial-score exchange, double-buffered: the (quantised) partial of tile
     // j goes to the peer's buffer j&1 and completes bytes on its barrier
-    // SX_FULL(j&1).
-    // A CTA sends tile j+1 only after it has consumed tile j, and it consumed
-    // tile j only after the peer had finished reading tile j-1 (the peer sent
-    // tile j after that read), so buffer (j+1)&1 is always free when written.
+    // SX_FULL(j&1).  A warp sends tile j+1 only after SX_FULL(j) completed and
+    // it has read tile j's values into registers.  SX_FULL(j) completing means
+    // every peer warp has sent tile j, which each did only after reading tile
+    // j-1 -- the tile whose buffer (j+1)&1 tile j+1 overwrites.
     const uint32_t sx_peer = mapa(base + kOffSx, peer);
     const uint32_t peer_sx_full = mapa(bar(B_SX_FULL0), peer);  // + 8 for buffer 1
+    const uint32_t sx_row = uint32_t(h * ROWS + rr) * uint32_t(NCOL * 2);  // this thread's data row
+    const uint32_t sx_sw = (uint32_t(rr) >> 2) & uint32_t(XU - 1);       // 16-byte unit swizzle
     float m_ref = -INFINITY, l = 0.f;
     bool alive = true;
-    uint32_t s[32];  // this CTA's partial scores of the tile being finished
+    uint32_t s[NCOL];  // this CTA's partial scores of the tile being finished
 
-    // load tile jn's partial scores from TMEM and send them to the peer as
-    // 32 int16 with a shared exponent k: q = rint(v * 2^(14-k)), max|v| < 2^k
+    // Load tile jn's partial scores from TMEM and send them to the peer as
+    // NCOL 16-bit integers with a shared exponent k (max|v| < 2^k):
+    // u = rint(v * 2^(14-k)) + 2^15.  The rounding is done by the adder: for
+    // |y| <= 2^14, y + (1.5*2^23 + 2^15) lands in [2^23, 2^24), where the float
+    // spacing is 1, and its low 16 mantissa bits are rint(y) + 2^15.  The
+    // receiver rebuilds 1.5*2^23 + u as float bits and subtracts exactly.
     auto fetch_and_send = [&](int jn) -> bool {
-      bool ok = wait_bar(bar(B_S_FULL), jn & 1, ctl, P.err, false);
+      bool ok = wait_fast(bar(B_S_FULL), jn & 1, ctl, P.err);
       if (!__all_sync(0xffffffffu, ok)) return false;
       if (tracer) MTV_TR(2, jn, 0);
       tc_fence_after();
-      tmem_ld32_sync(tmem + lane_off + kTmemS + 32 * h, s);
+      tmem_ld16_sync(tmem + lane_off + kTmemS + NCOL * h, s);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_S_FREE));
       float amax = 0.f;
 #pragma unroll
-      for (int u = 0; u < 32; u += 2)
+      for (int u = 0; u < NCOL; u += 2)
         amax = max3(amax, fabsf(__uint_as_float(s[u])), fabsf(__uint_as_float(s[u + 1])));
-      int k = 0;
-      frexpf(amax, &k);                  // amax < 2^k (0 -> k = 0)
+      // amax in [2^(k-1), 2^k) for normal amax; 0 and subnormals give k <= -126
+      int k = int((__float_as_uint(amax) >> 23) & 0xffu) - 126;
       k = max(-100, min(k, 100));
       const float qs = __int_as_float((127 + 14 - k) << 23);  // 2^(14-k), exact
-      uint32_t w[16];
-#pragma unroll
-      for (int u = 0; u < 16; ++u) {
-        const int a = __float2int_rn(__uint_as_float(s[2 * u]) * qs);
-        const int b = __float2int_rn(__uint_as_float(s[2 * u + 1]) * qs);
-        w[u] = (uint32_t(a) & 0xffffu) | (uint32_t(b) << 16);
-      }
+      const uint64_t qs2 = f2_pack(qs, qs), mg2 = f2_pack(kQuantMagic, kQuantMagic);
       const uint32_t buf = uint32_t(jn & 1) * kSxStride;
       const uint32_t pbar = peer_sx_full + 8u * uint32_t(jn & 1);
-      const uint32_t drow = sx_peer + buf + uint32_t(h) * (ROWS * 64) + uint32_t(rr) * 64u;
 #pragma unroll
-      for (int u = 0; u < 4; ++u)
-        st_async_v4(drow + ((uint32_t(u) ^ ((uint32_t(rr) >> 1) & 3u)) << 4), w[4 * u], w[4 * u + 1], w[4 * u + 2],
-                    w[4 * u + 3], pbar);
+      for (int u = 0; u < XU; ++u) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int c0 = 8 * u + 2 * e;
+          float a, b;
+          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c0]), __uint_as_float(s[c0 + 1])), qs2, mg2), a, b);
+          w[e] = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x5410);
+        }
+        st_async_v4(sx_peer + buf + sx_row + ((uint32_t(u) ^ sx_sw) << 4), w[0], w[1], w[2], w[3], pbar);
+      }
       st_async_b32(sx_peer + buf + kSxDataBytes + uint32_t(h * ROWS + rr) * 4u, uint32_t(k), pbar);
       if (tracer) MTV_TR(2, jn, 1);
       return true;
@@ -430,31 +452,40 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     for (int j = 0; alive && j < T; ++j) {
       // tile j+1's bytes land in buffer (j+1)&1, whose previous phase (tile j-1) is complete
       if (tracer && j + 1 < T) mbar_arrive_expect_tx(bar(B_SX_FULL0 + ((j + 1) & 1)), kSxBytes);
-      bool ok = wait_bar(bar(B_SX_FULL0 + (j & 1)), (j >> 1) & 1, ctl, P.err, false);
+      bool ok = wait_fast(bar(B_SX_FULL0 + (j & 1)), (j >> 1) & 1, ctl, P.err);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
       if (tracer) MTV_TR(2, j, 2);
-      float x[32];  // full scores of this warp's 32 columns: own exact partial + peer's
+      float x[NCOL];  // full scores of this warp's columns: own exact partial + peer's
       {
         const unsigned char* rxb = gbase + kOffSx + (j & 1) * kSxStride;
         const int kp = *reinterpret_cast<const int*>(rxb + kSxDataBytes + (h * ROWS + rr) * 4);
         const float dq = __int_as_float((127 - 14 + kp) << 23);  // 2^(k-14)
-        const uint4* row = reinterpret_cast<const uint4*>(rxb + h * (ROWS * 64) + rr * 64);
+        const uint64_t dq2 = f2_pack(dq, dq), nmg2 = f2_pack(-kQuantMagic, -kQuantMagic);
+        const uint4* row = reinterpret_cast<const uint4*>(rxb + sx_row);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const uint4 v = row[u ^ ((rr >> 1) & 3)];
+        for (int u = 0; u < XU; ++u) {
+          const uint4 v = row[u ^ sx_sw];
           const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            const int lo = int(wv[e] << 16) >> 16, hi = int(wv[e]) >> 16;
-            x[8 * u + 2 * e] = fmaf(float(lo), dq, __uint_as_float(s[8 * u + 2 * e]));
-            x[8 * u + 2 * e + 1] = fmaf(float(hi), dq, __uint_as_float(s[8 * u + 2 * e + 1]));
+            const int c0 = 8 * u + 2 * e;
+            const float flo = __uint_as_float(__byte_perm(wv[e], 0x4B40u, 0x5410));  // 1.5*2^23 + u_lo
+            const float fhi = __uint_as_float(__byte_perm(wv[e], 0x4B40u, 0x5432));  // 1.5*2^23 + u_hi
+            const uint64_t t2 = f2_add(f2_pack(flo, fhi), nmg2);                     // exact integers
+            f2_unpack(f2_fma(t2, dq2, f2_pack(__uint_as_float(s[c0]), __uint_as_float(s[c0 + 1]))), x[c0],
+                      x[c0 + 1]);
           }
         }
       }
+      // x now holds every value read from buffer j&1 (the empty asm orders the
+      // reads before the send below), so tile j+1 may be sent into buffer (j+1)&1.
+#pragma unroll
+      for (int cc = 0; cc < NCOL; ++cc) asm volatile("" : "+f"(x[cc]));
+      if (j + 1 < T && !fetch_and_send(j + 1)) { alive = false; break; }
 
       // tree mask (raw units; masked -> -inf)
       const int sidx = j % STAGES;
-      ok = wait_bar(bar(B_KV_FULL + sidx), (j / STAGES) & 1, ctl, P.err, false);
+      ok = wait_fast(bar(B_KV_FULL + sidx), (j / STAGES) & 1, ctl, P.err);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
       uint64_t vm = 0;  // OR of the gather warps' masks (exactly NPROD_WARPS words are written)
       {
@@ -466,11 +497,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         }
         if (NPROD_WARPS & 1) vm |= vmask_all[sidx * 8 + NPROD_WARPS - 1];
       }
-      const uint32_t vbits = uint32_t(vm >> (32 * h));
-      const int64_t kt = k_begin + int64_t(j) * NK + 32 * h;  // key of this warp's first column
-      if (!(valid && vbits == 0xffffffffu && kt + 32 <= R.p)) {  // not an all-prefix, all-valid tile
+      const uint32_t vbits = uint32_t(vm >> (NCOL * h)) & ((1u << NCOL) - 1u);
+      const int64_t kt = k_begin + int64_t(j) * NK + NCOL * h;  // key of this warp's first column
+      if (!(valid && vbits == ((1u << NCOL) - 1u) && kt + NCOL <= R.p)) {  // not an all-prefix, all-valid tile
 #pragma unroll
-        for (int cc = 0; cc < 32; ++cc) {
+        for (int cc = 0; cc < NCOL; ++cc) {
           const int64_t k = kt + cc;
           bool vis = valid && ((vbits >> cc) & 1u);
           if (vis && k >= R.p) vis = tree_visible(P, R, ti, k - R.p);
@@ -479,18 +510,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       }
       float mt = -INFINITY;
 #pragma unroll
-      for (int cc = 0; cc < 32; cc += 2) mt = max3(mt, x[cc], x[cc + 1]);
-      // The tile max depends on every value read from the exchange buffer, so
-      // once it is stored those reads are complete and tile j+1 may be sent
-      // (the peer writes our buffer j&1 again only after receiving it).
-      rowmax[((j & 1) * 2 + h) * ROWS + rr] = mt;
-      if (j + 1 < T && !fetch_and_send(j + 1)) { alive = false; break; }
-      // combine the tile max of the two halves of this row (bounded mbarrier meeting)
+      for (int cc = 0; cc < NCOL; cc += 2) mt = max3(mt, x[cc], x[cc + 1]);
+      rowmax[((j & 1) * WPQ + h) * ROWS + rr] = mt;
+      // combine the tile max of the WPQ warps of this row (bounded mbarrier meeting)
       __syncwarp();
       if (lane == 0) mbar_arrive(qbar);
-      ok = wait_bar(qbar, j & 1, ctl, P.err, false);
+      ok = wait_fast(qbar, j & 1, ctl, P.err);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
-      mt = fmaxf(mt, rowmax[((j & 1) * 2 + (h ^ 1)) * ROWS + rr]);
+#pragma unroll
+      for (int hh = 0; hh < WPQ; ++hh) mt = fmaxf(mt, rowmax[((j & 1) * WPQ + hh) * ROWS + rr]);
       if (tracer) MTV_TR(2, j, 3);
 
       const float m_new = fmaxf(m_ref, mt);
@@ -503,9 +531,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
       const uint64_t c2 = f2_pack(c, c), nb2 = f2_pack(nb, nb);
       uint64_t lsum2 = f2_pack(0.f, 0.f);
-      uint32_t pk[16];
+      uint32_t pk[NCOL / 2];
 #pragma unroll
-      for (int u = 0; u < 16; ++u) {
+      for (int u = 0; u < NCOL / 2; ++u) {
         float e0, e1;
         f2_unpack(f2_fma(f2_pack(x[2 * u], x[2 * u + 1]), c2, nb2), e0, e1);
         const float p0 = ex2(e0), p1 = ex2(e1);
@@ -522,15 +550,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       // P buffer j&1 was last read by GEMM2(j-2); O may only be rescaled once
       // GEMM2(j-1) has finished accumulating into it.
       if (j >= 2) {
-        ok = wait_bar(bar(B_O_READY0 + (j & 1)), ((j - 2) >> 1) & 1, ctl, P.err, false);
+        ok = wait_fast(bar(B_O_READY0 + (j & 1)), ((j - 2) >> 1) & 1, ctl, P.err);
         if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
       }
-      if (j >= 1 && __any_sync(0xffffffffu, move)) {  // warp-uniform TMEM read-modify-write of this warp's O half
-        ok = wait_bar(bar(B_O_READY0 + ((j - 1) & 1)), ((j - 1) >> 1) & 1, ctl, P.err, false);
+      if (j >= 1 && __any_sync(0xffffffffu, move)) {  // warp-uniform TMEM read-modify-write of this warp's O columns
+        ok = wait_fast(bar(B_O_READY0 + ((j - 1) & 1)), ((j - 1) >> 1) & 1, ctl, P.err);
         if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
         tc_fence_after();
 #pragma unroll 1
-        for (int c0 = 128 * h; c0 < 128 * h + 128; c0 += 32) {
+        for (int c0 = OCOLS * h; c0 < OCOLS * h + OCOLS; c0 += 32) {
           uint32_t v[32];
           tmem_ld32_sync(tmem + lane_off + kTmemO + c0, v);
 #pragma unroll
@@ -540,40 +568,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       }
       tc_fence_after();
       if (tracer) MTV_TR(2, j, 4);
-      tmem_st16_sync(tmem + lane_off + kTmemP + 32 * (j & 1) + 16 * h, pk);
+      tmem_st8_sync(tmem + lane_off + kTmemP + 32 * (j & 1) + (NCOL / 2) * h, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (j & 1)));
       if (tracer) MTV_TR(2, j, 5);
     }
 
-    // epilogue: normalised O half (+ LSE from CTA 0)
+    // epilogue: normalised O columns of this warp (+ LSE from CTA 0, warp h = 0)
     if (alive) {
-      bool ok = wait_bar(bar(B_O_READY0 + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl, P.err, false);
+      bool ok = wait_fast(bar(B_O_READY0 + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl, P.err);
       alive = __all_sync(0xffffffffu, ok);
     }
-    // the row's two partial sums (one per half) meet in shared memory: half 1
-    // publishes, half 0 adds, both read the total
+    // the row's WPQ partial sums meet in shared memory
     if (alive) {
-      if (h == 1) lsum_s[rr] = l;
+      lsum_s[h * ROWS + rr] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(qbar);
-      bool ok = wait_bar(qbar, T & 1, ctl, P.err, false);
+      bool ok = wait_fast(qbar, T & 1, ctl, P.err);
       alive = __all_sync(0xffffffffu, ok);
     }
     if (alive) {
-      if (h == 0) lsum_s[rr] += l;
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qbar);
-      bool ok = wait_bar(qbar, (T + 1) & 1, ctl, P.err, false);
-      alive = __all_sync(0xffffffffu, ok);
-    }
-    if (alive) {
-      const float tot = lsum_s[rr];
+      float tot = 0.f;
+#pragma unroll
+      for (int hh = 0; hh < WPQ; ++hh) tot += lsum_s[hh * ROWS + rr];
       tc_fence_after();
       const float inv = tot > 0.f ? 1.f / tot : 0.f;
 #pragma unroll 1
-      for (int c0 = 128 * h; c0 < 128 * h + 128; c0 += 32) {
+      for (int c0 = OCOLS * h; c0 < OCOLS * h + OCOLS; c0 += 32) {
         uint32_t v[32];
         tmem_ld32_sync(tmem + lane_off + kTmemO + c0, v);
         if (!valid) continue;
