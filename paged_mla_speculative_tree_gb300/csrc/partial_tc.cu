@@ -21,8 +21,9 @@
 //   2. GEMM1 on the tensor core: S_c[128 x 64] = Q_c . K_c^T, fp32 in TMEM;
 //      the latent part of Q_c is the A operand in TMEM (16 k-steps), its rope
 //      part an A operand in shared memory (2 k-steps);
-//   3. the softmax warps send their partial S to the peer CTA with st.async
-//      (completing bytes on the peer's barrier, double-buffered, one tile
+//   3. the softmax warps send their partial S to the peer CTA (each warp
+//      stages its 32 rows in shared memory and issues one bulk copy that
+//      completes bytes on the peer's barrier; double-buffered, one tile
 //      ahead) as 16-bit integers with one power-of-two exponent per 16 values
 //      (block floating point: error <= 2^-15 of the block's largest
 //      magnitude; the distributed-shared-memory link, not the arithmetic, is
@@ -83,14 +84,18 @@ constexpr uint32_t kChunkBytes = NK * 128;                       // 64 latent di
 constexpr uint32_t kRopeBytes = NK * 64;                          // 32 rope dims x 64 keys
 constexpr uint32_t kStageBytes = 4 * kChunkBytes + kRopeBytes;    // 36 KB
 constexpr uint32_t kOffStages = 0;
-// Peer's partial S, 2 buffers of [warp h][row] x (NCOL int16) + [warp h][row] exponents.
-constexpr uint32_t kOffSx = kOffStages + STAGES * kStageBytes;
-constexpr uint32_t kSxDataBytes = WPQ * ROWS * NCOL * 2;
-constexpr uint32_t kSxBytes = kSxDataBytes + WPQ * ROWS * 4;      // bytes completed per tile
-constexpr uint32_t kSxStride = (kSxBytes + 1023) & ~1023u;
-constexpr uint32_t kOffQRope = kOffSx + 2 * kSxStride;            // rope part of Q, 64B-swizzled
+constexpr uint32_t kOffQRope = kOffStages + STAGES * kStageBytes;  // rope part of Q, 64B-swizzled
 constexpr uint32_t kQRopeBytes = ROWS * 64;
-constexpr uint32_t kOffVmask = kOffQRope + kQRopeBytes;           // [stage][8] key validity masks
+// Partial-score exchange.  One region per softmax warp: its 32 rows x NCOL
+// int16 (32 B per row, 16-byte units swizzled) followed by one int8 exponent
+// per row.  Two receive buffers (written by the peer) and two send buffers
+// (staging for the bulk copies), each NSOFT_WARPS regions.
+constexpr uint32_t kXRowBytes = NCOL * 2;
+constexpr uint32_t kXRegion = 32 * kXRowBytes + 32;                 // 1056
+constexpr uint32_t kXBytes = NSOFT_WARPS * kXRegion;               // bytes completed per tile
+constexpr uint32_t kOffRx = kOffQRope + kQRopeBytes;
+constexpr uint32_t kOffTx = kOffRx + 2 * kXBytes;
+constexpr uint32_t kOffVmask = kOffTx + 2 * kXBytes;                // [stage][8] key validity masks
 constexpr uint32_t kVmaskBytes = STAGES * 8 * 8;
 constexpr uint32_t kOffRowMax = kOffVmask + kVmaskBytes;          // [2 tiles][WPQ][128 rows] f32
 constexpr uint32_t kRowMaxBytes = 2 * WPQ * ROWS * 4;
@@ -111,6 +116,7 @@ static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kOffQRope % 1024 == 0, "64B-swizzled operand alignment");
 static_assert(NPROD_WARPS <= 8, "one 64-bit validity word per gather warp, 8 per stage");
 static_assert(NCOL % 8 == 0 && XU >= 1 && (XU & (XU - 1)) == 0, "softmax column split");
+static_assert(kXRegion % 16 == 0 && kOffRx % 16 == 0 && kOffTx % 16 == 0, "bulk copy alignment");
 
 struct Ctl {
   uint32_t tmem_base;
@@ -191,7 +197,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     mbar_init(bar(B_O_READY0), 1);
     mbar_init(bar(B_O_READY1), 1);
     mbar_init(bar(B_Q_READY), NSOFT_WARPS);
-    mbar_init(bar(B_SX_FULL0), 1);  // one local expect_tx arrival + the peer's st.async bytes
+    mbar_init(bar(B_SX_FULL0), 1);  // one local expect_tx arrival + the peer's bulk-copy bytes
     mbar_init(bar(B_SX_FULL1), 1);
     mbar_init(bar(B_FIN), 1);
     for (int qq = 0; qq < 4; ++qq) mbar_init(bar(B_QMAX + qq), WPQ);
@@ -213,36 +219,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     if (lane == 0) {
       const uint32_t id1 = idesc_bf16_f32(128, NK, 0, 0);
       const uint32_t id2 = idesc_bf16_f32(128, 256, 0, 1);
-      // GEMM2 of tile jj: P from TMEM buffer jj&1, V from the tile's stage.
-      auto gemm2 = [&](int jj) -> bool {
-        if (!wait_bar(bar(B_P_FULL0 + (jj & 1)), (jj >> 1) & 1, ctl, P.err, false)) return false;
-        MTV_TR(0, jj, 2);
-        tc_fence_after();
-        const uint32_t st = base + kOffStages + uint32_t(jj % STAGES) * kStageBytes;
-        const uint32_t pa = tmem + kTmemP + 32u * uint32_t(jj & 1);
-#pragma unroll
-        for (int kk = 0; kk < KSTEPS2; ++kk) {
-          const uint64_t bd = smem_desc(st + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
-          mma_ts(tmem + kTmemO, pa + kk * 8, bd, id2, (jj > 0 || kk > 0) ? 1u : 0u);
-        }
-        mma_commit(bar(B_O_READY0 + (jj & 1)));
-        mma_commit(bar(B_KV_EMPTY + jj % STAGES));
-        return true;
-      };
-      // GEMM1 of tile j is issued as soon as its stage has landed and the
-      // softmax has read S(j-1); GEMM2 trails by two tiles, so the softmax of
-      // tile j finds S(j+1) already computed when it fetches it.
-      bool ok = wait_bar(bar(B_Q_READY), 0, ctl, P.err, false);
-      for (int j = 0; ok && j < T; ++j) {
-        const int s = j % STAGES;
-        ok = wait_bar(bar(B_KV_FULL + s), (j / STAGES) & 1, ctl, P.err, false);
-        MTV_TR(0, j, 0);
-        if (ok && j > 0) ok = wait_bar(bar(B_S_FREE), (j - 1) & 1, ctl, P.err, false);
-        if (!ok) break;
-        MTV_TR(0, j, 1);
+      // GEMM1 of tile j: S = Q . K^T into the single S buffer.
+      auto gemm1 = [&](int jj) {
+        MTV_TR(0, jj, 1);
         fence_proxy_async_smem();  // cp.async wrote the stage through the generic proxy
         tc_fence_after();
-        const uint32_t st = base + kOffStages + uint32_t(s) * kStageBytes;
+        const uint32_t st = base + kOffStages + uint32_t(jj % STAGES) * kStageBytes;
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
           const uint64_t bd = smem_desc(st + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024, kSwizzle128B);
@@ -255,10 +237,56 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
           mma_ss(tmem + kTmemS, ad, bd, id1, 1u);
         }
         mma_commit(bar(B_S_FULL));
-        if (j >= 2) ok = gemm2(j - 2);
+      };
+      // GEMM2 of tile j: O += P . V, P from TMEM buffer j&1, V from the tile's stage.
+      auto gemm2 = [&](int jj) {
+        MTV_TR(0, jj, 2);
+        tc_fence_after();
+        const uint32_t st = base + kOffStages + uint32_t(jj % STAGES) * kStageBytes;
+        const uint32_t pa = tmem + kTmemP + 32u * uint32_t(jj & 1);
+#pragma unroll
+        for (int kk = 0; kk < KSTEPS2; ++kk) {
+          const uint64_t bd = smem_desc(st + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
+          mma_ts(tmem + kTmemO, pa + kk * 8, bd, id2, (jj > 0 || kk > 0) ? 1u : 0u);
+        }
+        mma_commit(bar(B_O_READY0 + (jj & 1)));
+        mma_commit(bar(B_KV_EMPTY + jj % STAGES));
+      };
+      // Event-driven issue: GEMM1(j1) as soon as its stage has landed and the
+      // softmax has read S(j1-1); GEMM2(j2) as soon as P(j2) is in TMEM.  The
+      // two streams never wait on each other's inputs, so a late stage does
+      // not hold back the GEMM2 that frees an earlier one.  Tensor-core
+      // operations of one thread run in issue order, and GEMM2(j) is only
+      // issued after GEMM1(j).
+      bool ok = wait_bar(bar(B_Q_READY), 0, ctl, P.err, false);
+      int j1 = 0, j2 = 0;
+      long long t_prog = clock64();
+      while (ok && j2 < T) {
+        bool did = false;
+        if (j1 < T && mbar_test_wait(bar(B_KV_FULL + j1 % STAGES), (j1 / STAGES) & 1) &&
+            (j1 == 0 || mbar_test_wait(bar(B_S_FREE), (j1 - 1) & 1))) {
+          MTV_TR(0, j1, 0);
+          gemm1(j1);
+          ++j1;
+          did = true;
+        }
+        if (j2 < j1 && mbar_test_wait(bar(B_P_FULL0 + (j2 & 1)), (j2 >> 1) & 1)) {
+          gemm2(j2);
+          ++j2;
+          did = true;
+        }
+        if (did) {
+          t_prog = clock64();
+        } else {
+          if (ctl->abort) break;
+          if (clock64() - t_prog > kTimeoutCycles) {
+            ctl->abort = 1;
+            atomicOr(P.err, MTV_DEVERR_TIMEOUT);
+            break;
+          }
+          __nanosleep(32);
+        }
       }
-      if (ok && T >= 2) ok = gemm2(T - 2);
-      if (ok) gemm2(T - 1);
       mma_commit(bar(B_FIN));  // drains every MMA issued above
       wait_bar(bar(B_FIN), 0, ctl, P.err, false);
     }
@@ -349,6 +377,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     float* rowmax = reinterpret_cast<float*>(gbase + kOffRowMax);  // [tile&1][h][row]
     float* lsum_s = reinterpret_cast<float*>(gbase + kOffLsum);    // [h][row]
     const bool tracer = (sw == 0 && lane == 0);
+    const bool tracer2 = (sw == NSOFT_WARPS - 1 && lane == 0);
     // Scores stay in raw (unscaled) units; the scale enters once per element in
     // the exponent: p = 2^(x*c - m*c) with c = scale*log2(e).
     const float c = P.scale_log2;
@@ -390,16 +419,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       if (lane == 0) mbar_arrive(bar(B_Q_READY));
     }
 
-    // Partial-score exchange, double-buffered: the (quantised) partial of tile
-    // j goes to the peer's buffer j&1 and completes bytes on its barrier
-    // SX_FULL(j&1).  A warp sends tile j+1 only after SX_FULL(j) completed and
-    // it has read tile j's values into registers.  SX_FULL(j) completing means
-    // every peer warp has sent tile j, which each did only after reading tile
-    // j-1 -- the tile whose buffer (j+1)&1 tile j+1 overwrites.
-    const uint32_t sx_peer = mapa(base + kOffSx, peer);
+    // Partial-score exchange, double-buffered: each warp stages the quantised
+    // partial of tile j for its 32 rows in send buffer j&1 and bulk-copies the
+    // region to the peer's receive buffer j&1, completing bytes on the peer's
+    // barrier SX_FULL(j&1).  A warp sends tile j+1 only after SX_FULL(j)
+    // completed and it has read tile j's values into registers.  SX_FULL(j)
+    // completing means every peer warp has sent tile j, which each did only
+    // after (a) reading tile j-1 -- the tile whose receive buffer (j+1)&1 tile
+    // j+1 overwrites -- and (b) seeing SX_FULL(j-1) complete, i.e. our bulk
+    // copies of tile j-1 had landed, so send buffer (j+1)&1 is free again.
+    const int wreg = h * 4 + q;                               // region of this warp (same in both CTAs)
+    const uint32_t x_lane = uint32_t(wreg) * kXRegion + uint32_t(lane) * kXRowBytes;
+    const uint32_t x_exp = uint32_t(wreg) * kXRegion + 32u * kXRowBytes + uint32_t(lane);
+    const uint32_t x_sw = (uint32_t(lane) >> 2) & uint32_t(XU - 1);  // 16-byte unit swizzle
+    const uint32_t rx_peer = mapa(base + kOffRx, peer) + uint32_t(wreg) * kXRegion;
     const uint32_t peer_sx_full = mapa(bar(B_SX_FULL0), peer);  // + 8 for buffer 1
-    const uint32_t sx_row = uint32_t(h * ROWS + rr) * uint32_t(NCOL * 2);  // this thread's data row
-    const uint32_t sx_sw = (uint32_t(rr) >> 2) & uint32_t(XU - 1);       // 16-byte unit swizzle
     float m_ref = -INFINITY, l = 0.f;
     bool alive = true;
     uint32_t s[NCOL];  // this CTA's partial scores of the tile being finished
@@ -416,6 +450,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       if (tracer) MTV_TR(2, jn, 0);
       tc_fence_after();
       tmem_ld16_sync(tmem + lane_off + kTmemS + NCOL * h, s);
+      if (tracer) MTV_TR(2, jn, 6);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_S_FREE));
@@ -428,8 +463,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       k = max(-100, min(k, 100));
       const float qs = __int_as_float((127 + 14 - k) << 23);  // 2^(14-k), exact
       const uint64_t qs2 = f2_pack(qs, qs), mg2 = f2_pack(kQuantMagic, kQuantMagic);
-      const uint32_t buf = uint32_t(jn & 1) * kSxStride;
-      const uint32_t pbar = peer_sx_full + 8u * uint32_t(jn & 1);
+      const uint32_t tx = base + kOffTx + uint32_t(jn & 1) * kXBytes;
 #pragma unroll
       for (int u = 0; u < XU; ++u) {
         uint32_t w[4];
@@ -440,31 +474,38 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
           f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c0]), __uint_as_float(s[c0 + 1])), qs2, mg2), a, b);
           w[e] = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x5410);
         }
-        st_async_v4(sx_peer + buf + sx_row + ((uint32_t(u) ^ sx_sw) << 4), w[0], w[1], w[2], w[3], pbar);
+        st_shared_v4(tx + x_lane + ((uint32_t(u) ^ x_sw) << 4), w[0], w[1], w[2], w[3]);
       }
-      st_async_b32(sx_peer + buf + kSxDataBytes + uint32_t(h * ROWS + rr) * 4u, uint32_t(k), pbar);
+      st_shared_u8(tx + x_exp, uint32_t(k));
+      fence_proxy_async_smem();  // the bulk copy reads the staging through the async proxy
+      __syncwarp();
+      if (lane == 0)
+        bulk_copy_to_peer(rx_peer + uint32_t(jn & 1) * kXBytes, tx + uint32_t(wreg) * kXRegion, kXRegion,
+                          peer_sx_full + 8u * uint32_t(jn & 1));
       if (tracer) MTV_TR(2, jn, 1);
+      if (tracer2) MTV_TR(3, jn, 1);
       return true;
     };
 
-    if (tracer) mbar_arrive_expect_tx(bar(B_SX_FULL0), kSxBytes);  // tile 0
+    if (tracer) mbar_arrive_expect_tx(bar(B_SX_FULL0), kXBytes);  // tile 0
     alive = fetch_and_send(0);
     for (int j = 0; alive && j < T; ++j) {
       // tile j+1's bytes land in buffer (j+1)&1, whose previous phase (tile j-1) is complete
-      if (tracer && j + 1 < T) mbar_arrive_expect_tx(bar(B_SX_FULL0 + ((j + 1) & 1)), kSxBytes);
+      if (tracer && j + 1 < T) mbar_arrive_expect_tx(bar(B_SX_FULL0 + ((j + 1) & 1)), kXBytes);
       bool ok = wait_fast(bar(B_SX_FULL0 + (j & 1)), (j >> 1) & 1, ctl, P.err);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
       if (tracer) MTV_TR(2, j, 2);
+      if (tracer2) MTV_TR(3, j, 2);
       float x[NCOL];  // full scores of this warp's columns: own exact partial + peer's
       {
-        const unsigned char* rxb = gbase + kOffSx + (j & 1) * kSxStride;
-        const int kp = *reinterpret_cast<const int*>(rxb + kSxDataBytes + (h * ROWS + rr) * 4);
+        const unsigned char* rxb = gbase + kOffRx + (j & 1) * kXBytes;
+        const int kp = *reinterpret_cast<const signed char*>(rxb + x_exp);
         const float dq = __int_as_float((127 - 14 + kp) << 23);  // 2^(k-14)
         const uint64_t dq2 = f2_pack(dq, dq), nmg2 = f2_pack(-kQuantMagic, -kQuantMagic);
-        const uint4* row = reinterpret_cast<const uint4*>(rxb + sx_row);
+        const uint4* row = reinterpret_cast<const uint4*>(rxb + x_lane);
 #pragma unroll
         for (int u = 0; u < XU; ++u) {
-          const uint4 v = row[u ^ sx_sw];
+          const uint4 v = row[u ^ x_sw];
           const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
@@ -481,12 +522,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       // reads before the send below), so tile j+1 may be sent into buffer (j+1)&1.
 #pragma unroll
       for (int cc = 0; cc < NCOL; ++cc) asm volatile("" : "+f"(x[cc]));
+      if (tracer) MTV_TR(2, j, 7);
       if (j + 1 < T && !fetch_and_send(j + 1)) { alive = false; break; }
 
       // tree mask (raw units; masked -> -inf)
       const int sidx = j % STAGES;
       ok = wait_fast(bar(B_KV_FULL + sidx), (j / STAGES) & 1, ctl, P.err);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+      if (tracer) MTV_TR(2, j, 8);
       uint64_t vm = 0;  // OR of the gather warps' masks (exactly NPROD_WARPS words are written)
       {
         const ulonglong2* vp = reinterpret_cast<const ulonglong2*>(vmask_all + sidx * 8);
@@ -512,6 +555,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
 #pragma unroll
       for (int cc = 0; cc < NCOL; cc += 2) mt = max3(mt, x[cc], x[cc + 1]);
       rowmax[((j & 1) * WPQ + h) * ROWS + rr] = mt;
+      if (tracer) MTV_TR(2, j, 9);
+      if (tracer2) MTV_TR(3, j, 9);
       // combine the tile max of the WPQ warps of this row (bounded mbarrier meeting)
       __syncwarp();
       if (lane == 0) mbar_arrive(qbar);
@@ -520,6 +565,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
 #pragma unroll
       for (int hh = 0; hh < WPQ; ++hh) mt = fmaxf(mt, rowmax[((j & 1) * WPQ + hh) * ROWS + rr]);
       if (tracer) MTV_TR(2, j, 3);
+      if (tracer2) MTV_TR(3, j, 3);
 
       const float m_new = fmaxf(m_ref, mt);
       const bool move = (m_new > m_ref + thr_raw) || (m_ref == -INFINITY && m_new != -INFINITY);
@@ -547,6 +593,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         l += a0 + a1;  // unrounded weights normalise O and give the LSE
       }
 
+      if (tracer) MTV_TR(2, j, 10);
       // P buffer j&1 was last read by GEMM2(j-2); O may only be rescaled once
       // GEMM2(j-1) has finished accumulating into it.
       if (j >= 2) {
@@ -573,6 +620,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (j & 1)));
       if (tracer) MTV_TR(2, j, 5);
+      if (tracer2) MTV_TR(3, j, 5);
     }
 
     // epilogue: normalised O columns of this warp (+ LSE from CTA 0, warp h = 0)
