@@ -1,10 +1,17 @@
-// Split-K combine: one warp per (token, head) row merges the per-split
-// normalised partial outputs by their log-sum-exp weights,
+// Split-K combine: merges the per-split normalised partial outputs of every
+// (token, head) row by their log-sum-exp weights,
 //   lse = ln sum_s exp(lse_s),   out = sum_s exp(lse_s - lse) * o_s,
 // and writes bf16 out (round-to-nearest-even) + fp32 lse.  The split count
 // of a request is re-derived on the device from its key count, so splits
 // past the request's end are never read ("The Final Solder Joint" -- "The
 // Three-Edits Sequence": empty splits early-out).
+//
+// One block per (tree token, 64-dim chunk of the output): 64 head rows x 64
+// dims.  The first 64 threads reduce the rows' split LSEs; then every thread
+// owns one float4 column of four rows and keeps the loads of two splits in
+// flight.  The kernel is launched as a programmatic dependent of the partial
+// kernel: everything before the grid-dependency wait (request geometry)
+// overlaps the partial kernel's tail.
 #include <math.h>
 
 #include "mtv_internal.cuh"
@@ -12,77 +19,99 @@
 namespace mtv {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kThreads = 256;
+constexpr int kChunkDims = 64;                 // output dims per block
+constexpr int kChunks = kDLat / kChunkDims;    // 8
+constexpr int kF4 = kChunkDims / 4;            // float4 columns per row chunk: 16
+constexpr int kRowsPerPass = kThreads / kF4;   // 16
+constexpr int kPasses = kHeads / kRowsPerPass; // 4 rows per thread
 
-__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const Params P) {
-  const int lane = threadIdx.x & 31;
-  const int64_t row = int64_t(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  const int64_t tok = row / kHeads;
-  if (P.bs <= 0 || tok >= P.total_q_max) return;
-  const int64_t total_q = P.qo_indptr[P.bs];
-  if (tok >= total_q) return;
-  // request owning this token: last r with qo_indptr[r] <= tok
-  int lo = 0, hi = P.bs - 1;
-  while (lo < hi) {
-    int mid = (lo + hi + 1) >> 1;
-    if (P.qo_indptr[mid] <= tok) lo = mid; else hi = mid - 1;
-  }
-  const int64_t p = int64_t(P.kv_indptr[lo + 1]) - P.kv_indptr[lo];
-  const int64_t n = P.qo_indptr[lo + 1] - P.qo_indptr[lo];
-  if (p < 0 || n < 0 || p > P.max_prefix || n > P.max_q) return;  // flagged by the partial kernel
-  const int ns = splits_used(P, p + n);
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__global__ void __launch_bounds__(kThreads) combine_kernel(const Params P) {
+  __shared__ float lse_row[kHeads];
+  const int r = int(blockIdx.x / unsigned(P.max_q));
+  const int t = int(blockIdx.x % unsigned(P.max_q));
+  const int chunk = int(blockIdx.y);
+  const Req R = load_req(P, r);
+  if (t >= R.n) return;
+  const int ns = splits_used(P, R.keys);
   const int64_t stride_rows = P.total_q_max * kHeads;
+  const int64_t row0 = (R.q_off + t) * kHeads;  // first (token, head) row of this block
+  grid_dependency_wait();                        // partials of the preceding kernel are complete
 
-  float m = -INFINITY;
-  for (int s = lane; s < ns; s += 32) m = fmaxf(m, P.part_lse[s * stride_rows + row]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const int tid = threadIdx.x;
+  if (tid < kHeads) {
+    const float* l = P.part_lse + row0 + tid;
+    float m = -INFINITY;
+    for (int s = 0; s < ns; ++s) m = fmaxf(m, l[s * stride_rows]);
+    float lse = -INFINITY;
+    if (m != -INFINITY) {
+      float sum = 0.f;
+      for (int s = 0; s < ns; ++s) sum += expf(l[s * stride_rows] - m);
+      lse = m + logf(sum);
+    }
+    lse_row[tid] = lse;
+    if (chunk == 0) P.lse[row0 + tid] = lse;
+  }
+  __syncthreads();
 
-  float acc[16];
+  const int f4 = tid % kF4;
+  const int rbase = tid / kF4;
+  float4 acc[kPasses];
+  float lr[kPasses];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) acc[j] = 0.f;
-  float lse = -INFINITY;
-  if (m != -INFINITY) {
-    float sum = 0.f;
-    for (int s = lane; s < ns; s += 32) sum += expf(P.part_lse[s * stride_rows + row] - m);
+  for (int i = 0; i < kPasses; ++i) {
+    acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+    lr[i] = lse_row[rbase + i * kRowsPerPass];
+  }
+  const int64_t col = int64_t(chunk) * kChunkDims + f4 * 4;
+#pragma unroll 2
+  for (int s = 0; s < ns; ++s) {
+    float4 v[kPasses];
+    float w[kPasses];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    lse = m + logf(sum);
-    for (int s = 0; s < ns; ++s) {
-      const float w = expf(P.part_lse[s * stride_rows + row] - lse);
-      if (w == 0.f) continue;
-      const float4* src = reinterpret_cast<const float4*>(P.part_o + (s * stride_rows + row) * kDLat) + lane * 4;
+    for (int i = 0; i < kPasses; ++i) {
+      const int64_t row = row0 + rbase + i * kRowsPerPass;
+      v[i] = *reinterpret_cast<const float4*>(P.part_o + (s * stride_rows + row) * kDLat + col);
+      w[i] = P.part_lse[s * stride_rows + row];
+    }
 #pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        float4 v = src[j];
-        acc[4 * j] = fmaf(w, v.x, acc[4 * j]);
-        acc[4 * j + 1] = fmaf(w, v.y, acc[4 * j + 1]);
-        acc[4 * j + 2] = fmaf(w, v.z, acc[4 * j + 2]);
-        acc[4 * j + 3] = fmaf(w, v.w, acc[4 * j + 3]);
-      }
+    for (int i = 0; i < kPasses; ++i) {
+      const float wi = lr[i] == -INFINITY ? 0.f : expf(w[i] - lr[i]);
+      acc[i].x = fmaf(wi, v[i].x, acc[i].x);
+      acc[i].y = fmaf(wi, v[i].y, acc[i].y);
+      acc[i].z = fmaf(wi, v[i].z, acc[i].z);
+      acc[i].w = fmaf(wi, v[i].w, acc[i].w);
     }
   }
-  uint4 packed[2];
-  uint32_t* pw = reinterpret_cast<uint32_t*>(packed);
 #pragma unroll
-  for (int j = 0; j < 8; ++j) {
-    __nv_bfloat162 b = __floats2bfloat162_rn(acc[2 * j], acc[2 * j + 1]);
-    pw[j] = *reinterpret_cast<uint32_t*>(&b);
+  for (int i = 0; i < kPasses; ++i) {
+    const int64_t row = row0 + rbase + i * kRowsPerPass;
+    const __nv_bfloat162 a = __floats2bfloat162_rn(acc[i].x, acc[i].y);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(acc[i].z, acc[i].w);
+    uint2 o;
+    o.x = *reinterpret_cast<const uint32_t*>(&a);
+    o.y = *reinterpret_cast<const uint32_t*>(&b);
+    *reinterpret_cast<uint2*>(P.out + row * kDLat + col) = o;
   }
-  uint4* dst = reinterpret_cast<uint4*>(P.out + row * kDLat) + lane * 2;
-  dst[0] = packed[0];
-  dst[1] = packed[1];
-  if (lane == 0) P.lse[row] = lse;
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const Params& P, cudaStream_t st) {
-  const int64_t rows = P.total_q_max * kHeads;
-  if (rows == 0 || P.bs == 0) return cudaSuccess;
-  const unsigned blocks = unsigned((rows + kWarps - 1) / kWarps);
-  combine_kernel<<<blocks, kWarps * 32, 0, st>>>(P);
-  return cudaGetLastError();
+  if (P.bs == 0 || P.max_q == 0) return cudaSuccess;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(unsigned(P.bs) * unsigned(P.max_q), unsigned(kChunks));
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, P);
 }
 
 }  // namespace mtv
