@@ -176,6 +176,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
   const int pair = blockIdx.x >> 1;
   const int r = pair / P.grid_rows, rb = pair % P.grid_rows;
   const int split = blockIdx.y;
+  if (threadIdx.x == 0) MTV_TR(1, kTraceTiles - 1, 0);
   const Req R = load_req(P, r);
   const int64_t rows_req = R.n * kHeads;
   if (int64_t(rb) * ROWS >= rows_req) return;  // both CTAs of the pair take this exit
@@ -184,6 +185,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
   const int64_t k_end = min(R.keys, k_begin + P.split_keys);
   const int T = int((k_end - k_begin + NK - 1) / NK);
   uint64_t* vmask_all = reinterpret_cast<uint64_t*>(gbase + kOffVmask);  // [stage][8]
+
+  // Slot of gather lane `lane` of warp `pw` for tile j (raw, checked at use).
+  auto raw_slot_of = [&](int pw, int j) -> int64_t {
+    int64_t v = -1;
+    const int nmine = (NK - pw + NPROD_WARPS - 1) / NPROD_WARPS;
+    if (lane < nmine && j < T) {
+      const int64_t k = k_begin + int64_t(j) * NK + pw + NPROD_WARPS * lane;
+      if (k < k_end) v = (k < R.p) ? P.kv_indices[R.kv_off + k] : P.out_cache_loc[R.q_off + (k - R.p)];
+    }
+    return v;
+  };
+  // The gather warps issue the index loads of their first two tiles before
+  // the setup below, so that the load latency overlaps it.
+  int64_t pre0 = -1, pre1 = -1;
+  if (warp >= 1 && warp <= NPROD_WARPS) {
+    pre0 = raw_slot_of(warp - 1, 0);
+    pre1 = raw_slot_of(warp - 1, 1);
+  }
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -212,6 +231,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
   __syncthreads();
   tc_fence_after();
   cluster_sync();  // barriers of both CTAs initialised before any remote access
+  if (threadIdx.x == 0) MTV_TR(1, kTraceTiles - 1, 1);
   const uint32_t tmem = ctl->tmem_base;
 
   if (warp == 0) {
@@ -313,15 +333,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     const unsigned char* pool_lat = reinterpret_cast<const unsigned char*>(P.kv_pool) + crank * 512 + lane * 16;
     const unsigned char* pool_rope =
         reinterpret_cast<const unsigned char*>(P.kv_pool) + 1024 + crank * 64 + (lane & 3) * 16;
-    auto raw_slot = [&](int j) -> int64_t {
-      int64_t v = -1;
-      if (lane < nmine && j < T) {
-        const int64_t k = k_begin + int64_t(j) * NK + pw + NPROD_WARPS * lane;
-        if (k < k_end) v = (k < R.p) ? P.kv_indices[R.kv_off + k] : P.out_cache_loc[R.q_off + (k - R.p)];
-      }
-      return v;
-    };
-    int64_t v0 = raw_slot(0), v1 = raw_slot(1);
+    int64_t v0 = pre0, v1 = pre1;
     for (int j = 0; j < T; ++j) {
       const int s = j % STAGES;
       int slot = -1;  // checked slot of this lane's key (< 2^31 by the ABI contract)
@@ -333,7 +345,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         }
       }
       v0 = v1;
-      v1 = raw_slot(j + 2);  // in flight until two iterations from now
+      v1 = raw_slot_of(pw, j + 2);  // in flight until two iterations from now
       const int kk_l = pw + NPROD_WARPS * lane;
       const uint32_t vlo = __reduce_or_sync(0xffffffffu, (slot >= 0 && kk_l < 32) ? 1u << kk_l : 0u);
       const uint32_t vhi = __reduce_or_sync(0xffffffffu, (slot >= 0 && kk_l >= 32) ? 1u << (kk_l - 32) : 0u);
@@ -623,6 +635,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       if (tracer2) MTV_TR(3, j, 5);
     }
 
+    if (tracer) MTV_TR(2, kTraceTiles - 1, 0);
     // epilogue: normalised O columns of this warp (+ LSE from CTA 0, warp h = 0)
     if (alive) {
       bool ok = wait_fast(bar(B_O_READY0 + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl, P.err);
@@ -642,32 +655,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       for (int hh = 0; hh < WPQ; ++hh) tot += lsum_s[hh * ROWS + rr];
       tc_fence_after();
       const float inv = tot > 0.f ? 1.f / tot : 0.f;
+      // Normalised O columns go through shared memory so that the global
+      // stores are row-contiguous: each thread holds one row, but a warp
+      // stores two rows x 256 bytes per instruction.  The staging uses the
+      // KV stage area, free once GEMM2(T-1) (the last tensor-core operation)
+      // has completed; 16-byte units are XOR-swizzled by row (conflict-free).
+      const uint32_t stg = base + kOffStages + uint32_t(sw) * (32u * OCOLS * 4u);  // 32 rows x OCOLS f32
 #pragma unroll 1
-      for (int c0 = OCOLS * h; c0 < OCOLS * h + OCOLS; c0 += 32) {
+      for (int c0 = 0; c0 < OCOLS; c0 += 32) {
         uint32_t v[32];
-        tmem_ld32_sync(tmem + lane_off + kTmemO + c0, v);
-        if (!valid) continue;
-        const int dcol = int(crank) * 256 + c0;
-        if (P.nsplit == 1) {
-          uint4* dst = reinterpret_cast<uint4*>(P.out + out_row * kDLat + dcol);
+        tmem_ld32_sync(tmem + lane_off + kTmemO + OCOLS * h + c0, v);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            uint32_t w[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const __nv_bfloat162 b = __floats2bfloat162_rn(__uint_as_float(v[8 * u + 2 * e]) * inv,
-                                                             __uint_as_float(v[8 * u + 2 * e + 1]) * inv);
-              w[e] = *reinterpret_cast<const uint32_t*>(&b);
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t unit = uint32_t(c0 / 4 + u);
+          st_shared_v4(stg + uint32_t(lane) * (OCOLS * 4u) + ((unit ^ (uint32_t(lane) & 15u)) << 4),
+                       __float_as_uint(__uint_as_float(v[4 * u]) * inv),
+                       __float_as_uint(__uint_as_float(v[4 * u + 1]) * inv),
+                       __float_as_uint(__uint_as_float(v[4 * u + 2]) * inv),
+                       __float_as_uint(__uint_as_float(v[4 * u + 3]) * inv));
+        }
+      }
+      __syncwarp();
+      {
+        const int half = lane >> 4;
+        const uint32_t unit = uint32_t(lane & 15);
+        const int dcol = int(crank) * 256 + OCOLS * h + int(unit) * 4;
+#pragma unroll 4
+        for (int pr = 0; pr < 16; ++pr) {
+          const int rl = 2 * pr + half;  // row within this warp's 32
+          const int64_t g = int64_t(rb) * ROWS + q * 32 + rl;
+          const float4 val = ld_shared_f4(stg + uint32_t(rl) * (OCOLS * 4u) + ((unit ^ (uint32_t(rl) & 15u)) << 4));
+          if (g < rows_req) {
+            const int64_t orow = R.q_off * kHeads + g;
+            if (P.nsplit == 1) {
+              const __nv_bfloat162 a = __floats2bfloat162_rn(val.x, val.y);
+              const __nv_bfloat162 b = __floats2bfloat162_rn(val.z, val.w);
+              *reinterpret_cast<uint2*>(P.out + orow * kDLat + dcol) =
+                  make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+            } else {
+              *reinterpret_cast<float4*>(P.part_o + (int64_t(split) * P.total_q_max * kHeads + orow) * kDLat + dcol) =
+                  val;
             }
-            dst[u] = make_uint4(w[0], w[1], w[2], w[3]);
           }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(
-              P.part_o + (int64_t(split) * P.total_q_max * kHeads + out_row) * kDLat + dcol);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            dst[u] = make_float4(__uint_as_float(v[4 * u]) * inv, __uint_as_float(v[4 * u + 1]) * inv,
-                                 __uint_as_float(v[4 * u + 2]) * inv, __uint_as_float(v[4 * u + 3]) * inv);
         }
       }
       if (valid && crank == 0 && h == 0) {
@@ -681,8 +710,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  if (threadIdx.x == 0) MTV_TR(2, kTraceTiles - 1, 2);
   if (warp == 0) tmem_dealloc(tmem, 512);
   cluster_sync();  // the peer may still arrive on / store into this CTA's shared memory until here
+  if (threadIdx.x == 0) MTV_TR(2, kTraceTiles - 1, 3);
 }
 
 }  // namespace
