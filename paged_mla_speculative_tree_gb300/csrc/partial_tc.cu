@@ -29,8 +29,8 @@
 //      magnitude; the distributed-shared-memory link, not the arithmetic, is
 //      what this exchange costs), add the peer's partial to their own exact
 //      one, apply the tree mask (prefix always visible, tree columns from
-//      custom_mask), and run the fp32 online softmax (four warps per row
-//      quarter, 16 key columns each; "Design Decisions and
+//      custom_mask), and run the fp32 online softmax (two warps per TMEM
+//      lane quarter, 32 key columns each; "Design Decisions and
 //      Trade-Offs": mask -> -inf, streaming max/sum) with a lazily moved
 //      reference max; P (bf16) goes to one of two TMEM buffers.  Each CTA
 //      normalises its own O half with its own softmax sums, so the two views
@@ -65,14 +65,18 @@ constexpr int ROWS = 128;   // query rows per CTA pair
 constexpr int NK = 64;      // keys per tile
 constexpr int STAGES = 4;   // gather pipeline depth
 #ifndef MTV_TC_GATHER_WARPS
-#define MTV_TC_GATHER_WARPS 3  // 3 + 16 + 1 warps leave 96 registers per thread
+#define MTV_TC_GATHER_WARPS 3
 #endif
 constexpr int NPROD_WARPS = MTV_TC_GATHER_WARPS;
-constexpr int NSOFT_WARPS = 16;            // four per TMEM lane quarter
+#ifndef MTV_TC_SOFTMAX_WARPS
+#define MTV_TC_SOFTMAX_WARPS 8
+#endif
+constexpr int NSOFT_WARPS = MTV_TC_SOFTMAX_WARPS;  // a multiple of 4: WPQ per TMEM lane quarter
 constexpr int WPQ = NSOFT_WARPS / 4;       // softmax warps sharing one lane quarter (one row)
-constexpr int NCOL = NK / WPQ;             // key columns per softmax warp: 16
-constexpr int OCOLS = 256 / WPQ;           // O columns per softmax warp (rescale, epilogue): 64
-constexpr int XU = NCOL * 2 / 16;          // 16-byte units of one thread's quantised partial row: 2
+constexpr int NCOL = NK / WPQ;             // key columns per softmax warp
+constexpr int OCOLS = 256 / WPQ;           // O columns per softmax warp (rescale, epilogue)
+constexpr int XU = NCOL * 2 / 16;          // 16-byte units of one thread's quantised partial row
+constexpr uint32_t kColMask = NCOL >= 32 ? 0xffffffffu : ((1u << NCOL) - 1u);
 constexpr int NTHREADS = 32 * (1 + NPROD_WARPS + NSOFT_WARPS);  // warp 0 MMA, then gather, then softmax
 constexpr int KSTEPS2 = NK / 16;          // 4
 constexpr float kRescaleLog2 = 8.0f;      // move the reference max only past 2^8 growth
@@ -115,7 +119,8 @@ static_assert(B_COUNT * 8 <= 256, "barrier area");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kOffQRope % 1024 == 0, "64B-swizzled operand alignment");
 static_assert(NPROD_WARPS <= 8, "one 64-bit validity word per gather warp, 8 per stage");
-static_assert(NCOL % 8 == 0 && XU >= 1 && (XU & (XU - 1)) == 0, "softmax column split");
+static_assert((NSOFT_WARPS == 8 || NSOFT_WARPS == 16) && NCOL % 8 == 0 && (XU & (XU - 1)) == 0,
+              "softmax column split");
 static_assert(kXRegion % 16 == 0 && kOffRx % 16 == 0 && kOffTx % 16 == 0, "bulk copy alignment");
 
 struct Ctl {
@@ -443,7 +448,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     const int wreg = h * 4 + q;                               // region of this warp (same in both CTAs)
     const uint32_t x_lane = uint32_t(wreg) * kXRegion + uint32_t(lane) * kXRowBytes;
     const uint32_t x_exp = uint32_t(wreg) * kXRegion + 32u * kXRowBytes + uint32_t(lane);
-    const uint32_t x_sw = (uint32_t(lane) >> 2) & uint32_t(XU - 1);  // 16-byte unit swizzle
+    // 16-byte unit swizzle: the rows sharing a 128-byte line get distinct unit orders
+    const uint32_t x_sw = (uint32_t(lane) / uint32_t(128 / kXRowBytes)) & uint32_t(XU - 1);
     const uint32_t rx_peer = mapa(base + kOffRx, peer) + uint32_t(wreg) * kXRegion;
     const uint32_t peer_sx_full = mapa(bar(B_SX_FULL0), peer);  // + 8 for buffer 1
     float m_ref = -INFINITY, l = 0.f;
@@ -461,7 +467,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       if (!__all_sync(0xffffffffu, ok)) return false;
       if (tracer) MTV_TR(2, jn, 0);
       tc_fence_after();
-      tmem_ld16_sync(tmem + lane_off + kTmemS + NCOL * h, s);
+      tmem_ld_sync(tmem + lane_off + kTmemS + NCOL * h, s);
       if (tracer) MTV_TR(2, jn, 6);
       tc_fence_before();
       __syncwarp();
@@ -552,9 +558,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         }
         if (NPROD_WARPS & 1) vm |= vmask_all[sidx * 8 + NPROD_WARPS - 1];
       }
-      const uint32_t vbits = uint32_t(vm >> (NCOL * h)) & ((1u << NCOL) - 1u);
+      const uint32_t vbits = uint32_t(vm >> (NCOL * h)) & kColMask;
       const int64_t kt = k_begin + int64_t(j) * NK + NCOL * h;  // key of this warp's first column
-      if (!(valid && vbits == ((1u << NCOL) - 1u) && kt + NCOL <= R.p)) {  // not an all-prefix, all-valid tile
+      if (!(valid && vbits == kColMask && kt + NCOL <= R.p)) {  // not an all-prefix, all-valid tile
 #pragma unroll
         for (int cc = 0; cc < NCOL; ++cc) {
           const int64_t k = kt + cc;
@@ -627,7 +633,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       }
       tc_fence_after();
       if (tracer) MTV_TR(2, j, 4);
-      tmem_st8_sync(tmem + lane_off + kTmemP + 32 * (j & 1) + (NCOL / 2) * h, pk);
+      tmem_st_sync(tmem + lane_off + kTmemP + 32 * (j & 1) + (NCOL / 2) * h, pk);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (j & 1)));
@@ -677,12 +683,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       }
       __syncwarp();
       {
-        const int half = lane >> 4;
-        const uint32_t unit = uint32_t(lane & 15);
+        constexpr int kUnits = OCOLS / 4;                       // 16-byte units per staged row
+        constexpr int kRowsPerPass = 32 / kUnits;               // rows one warp instruction covers
+        const int half = lane / kUnits;
+        const uint32_t unit = uint32_t(lane % kUnits);
         const int dcol = int(crank) * 256 + OCOLS * h + int(unit) * 4;
 #pragma unroll 4
-        for (int pr = 0; pr < 16; ++pr) {
-          const int rl = 2 * pr + half;  // row within this warp's 32
+        for (int pr = 0; pr < 32 / kRowsPerPass; ++pr) {
+          const int rl = kRowsPerPass * pr + half;  // row within this warp's 32
           const int64_t g = int64_t(rb) * ROWS + q * 32 + rl;
           const float4 val = ld_shared_f4(stg + uint32_t(rl) * (OCOLS * 4u) + ((unit ^ (uint32_t(rl) & 15u)) << 4));
           if (g < rows_req) {

@@ -243,6 +243,11 @@ __device__ __forceinline__ void tmem_st32_sync(uint32_t taddr, const uint32_t (&
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
+// Width-generic forms (the array size picks the shape).
+__device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, uint32_t (&v)[16]) { tmem_ld16_sync(taddr, v); }
+__device__ __forceinline__ void tmem_ld_sync(uint32_t taddr, uint32_t (&v)[32]) { tmem_ld32_sync(taddr, v); }
+__device__ __forceinline__ void tmem_st_sync(uint32_t taddr, const uint32_t (&v)[8]) { tmem_st8_sync(taddr, v); }
+__device__ __forceinline__ void tmem_st_sync(uint32_t taddr, const uint32_t (&v)[16]) { tmem_st16_sync(taddr, v); }
 
 // ---------------------------------------------------------------- packed fp32 (sm_100+)
 __device__ __forceinline__ uint64_t f2_pack(float a, float b) {
