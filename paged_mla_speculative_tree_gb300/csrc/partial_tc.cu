@@ -11,7 +11,7 @@
 //
 // The 576 contraction dims are split between the two CTAs: CTA c holds latent
 // dims [256c, 256c+256) and rope dims [32c, 32c+32).  Per 64-key tile:
-//   1. three gather warps copy the CTA's 576 bytes of each latent row with
+//   1. two gather warps copy the CTA's 576 bytes of each latent row with
 //      cp.async (16 B per lane, one row per warp instruction) into a
 //      128B-swizzled K-major tile (64B swizzle for the rope part); invalid
 //      slots are zero-filled; each lane's copies complete on the stage's
@@ -65,7 +65,7 @@ constexpr int ROWS = 128;   // query rows per CTA pair
 constexpr int NK = 64;      // keys per tile
 constexpr int STAGES = 4;   // gather pipeline depth
 #ifndef MTV_TC_GATHER_WARPS
-#define MTV_TC_GATHER_WARPS 3
+#define MTV_TC_GATHER_WARPS 2
 #endif
 constexpr int NPROD_WARPS = MTV_TC_GATHER_WARPS;
 #ifndef MTV_TC_SOFTMAX_WARPS
@@ -83,6 +83,7 @@ constexpr float kRescaleLog2 = 8.0f;      // move the reference max only past 2^
 constexpr float kQuantMagic = 12615680.0f;  // 1.5 * 2^23 + 2^15
 constexpr long long kTimeoutCycles = 1ll << 31;
 constexpr int kMaxKeysPerGatherWarp = (NK + NPROD_WARPS - 1) / NPROD_WARPS;
+constexpr int kRopeGroups = (kMaxKeysPerGatherWarp + 7) / 8;  // rope copies: 8 keys x 4 lanes per instruction
 
 constexpr uint32_t kChunkBytes = NK * 128;                       // 64 latent dims x 64 keys
 constexpr uint32_t kRopeBytes = NK * 64;                          // 32 rope dims x 64 keys
@@ -321,19 +322,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     // Warp pw copies keys pw, pw + NPROD_WARPS, ... of each tile.  Lane i
     // holds the slot of the warp's i-th key, loaded two tiles ahead and only
     // checked when used, so index latency never stalls the warp.  Per key the
-    // warp issues one 512-byte latent copy (32 lanes x 16 B) and one 64-byte
-    // rope copy (4 lanes) into the swizzled operand layout; an invalid slot is
-    // zero-filled (source size 0).  Each lane then arrives on the stage's
-    // barrier when its own copies land: the warp only waits for a free stage.
+    // warp issues one 512-byte latent copy (32 lanes x 16 B), and per group
+    // of 8 keys one copy of their 64-byte rope parts (4 lanes per key), into
+    // the swizzled operand layout; an invalid slot is zero-filled (source
+    // size 0).  Each lane then arrives on the stage's barrier when its own
+    // copies land: the warp only waits for a free stage.
     const int pw = warp - 1;
     const int nmine = (NK - pw + NPROD_WARPS - 1) / NPROD_WARPS;
     // per-key swizzled destination offsets within a stage (same for every tile)
-    uint32_t lat_off[kMaxKeysPerGatherWarp], rope_off[kMaxKeysPerGatherWarp];
+    uint32_t lat_off[kMaxKeysPerGatherWarp], rope_off[kRopeGroups];
 #pragma unroll
     for (int i = 0; i < kMaxKeysPerGatherWarp; ++i) {
       const int kk = pw + NPROD_WARPS * i;
       lat_off[i] = uint32_t(lane >> 3) * kChunkBytes + kk * 128 + (((lane & 7) ^ (kk & 7)) << 4);
-      rope_off[i] = 4 * kChunkBytes + kk * 64 + (((lane & 3) ^ ((kk >> 1) & 3)) << 4);
+    }
+#pragma unroll
+    for (int g = 0; g < kRopeGroups; ++g) {
+      const int kk = pw + NPROD_WARPS * (8 * g + (lane >> 2));
+      rope_off[g] = 4 * kChunkBytes + kk * 64 + (((lane & 3) ^ ((kk >> 1) & 3)) << 4);
     }
     const unsigned char* pool_lat = reinterpret_cast<const unsigned char*>(P.kv_pool) + crank * 512 + lane * 16;
     const unsigned char* pool_rope =
@@ -370,9 +376,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         if (i < nmine) {
           const int sl = __shfl_sync(0xffffffffu, slot, i);
           const int64_t row = int64_t(sl < 0 ? 0 : sl) * (kDQK * 2);
-          const uint32_t nbytes = sl >= 0 ? 16u : 0u;
-          cp_async_16_zfill(st + lat_off[i], pool_lat + row, nbytes);
-          if (lane < 4) cp_async_16_zfill(st + rope_off[i], pool_rope + row, nbytes);
+          cp_async_16_zfill(st + lat_off[i], pool_lat + row, sl >= 0 ? 16u : 0u);
+        }
+      }
+#pragma unroll
+      for (int g = 0; g < kRopeGroups; ++g) {
+        const int i = 8 * g + (lane >> 2);  // this lane's key in the group (< 32)
+        const int sl = __shfl_sync(0xffffffffu, slot, i);
+        if (i < nmine) {
+          const int64_t row = int64_t(sl < 0 ? 0 : sl) * (kDQK * 2);
+          cp_async_16_zfill(st + rope_off[g], pool_rope + row, sl >= 0 ? 16u : 0u);
         }
       }
       cp_async_arrive_noinc(fb);
