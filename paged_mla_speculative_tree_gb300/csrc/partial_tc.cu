@@ -63,7 +63,10 @@ using namespace ptx;
 
 constexpr int ROWS = 128;   // query rows per CTA pair
 constexpr int NK = 64;      // keys per tile
-constexpr int STAGES = 4;   // gather pipeline depth
+#ifndef MTV_TC_STAGES
+#define MTV_TC_STAGES 4  // shared memory holds four 36 KB stages next to the exchange buffers
+#endif
+constexpr int STAGES = MTV_TC_STAGES;  // gather pipeline depth
 #ifndef MTV_TC_GATHER_WARPS
 #define MTV_TC_GATHER_WARPS 2
 #endif
@@ -485,10 +488,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_S_FREE));
-      float amax = 0.f;
+      // (reductions run as four independent chains: the max instructions are opaque to the compiler)
+      float am[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int u = 0; u < NCOL; u += 2)
-        amax = max3(amax, fabsf(__uint_as_float(s[u])), fabsf(__uint_as_float(s[u + 1])));
+        am[(u >> 1) & 3] = max3(am[(u >> 1) & 3], fabsf(__uint_as_float(s[u])), fabsf(__uint_as_float(s[u + 1])));
+      const float amax = max3(fmaxf(am[0], am[1]), am[2], am[3]);
       // amax in [2^(k-1), 2^k) for normal amax; 0 and subnormals give k <= -126
       int k = int((__float_as_uint(amax) >> 23) & 0xffu) - 126;
       k = max(-100, min(k, 100));
@@ -582,9 +587,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
           if (!vis) x[cc] = -INFINITY;
         }
       }
-      float mt = -INFINITY;
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-      for (int cc = 0; cc < NCOL; cc += 2) mt = max3(mt, x[cc], x[cc + 1]);
+      for (int cc = 0; cc < NCOL; cc += 2) mx[(cc >> 1) & 3] = max3(mx[(cc >> 1) & 3], x[cc], x[cc + 1]);
+      float mt = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
       rowmax[((j & 1) * WPQ + h) * ROWS + rr] = mt;
       if (tracer) MTV_TR(2, j, 9);
       if (tracer2) MTV_TR(3, j, 9);
@@ -607,20 +613,22 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       }
       const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
       const uint64_t c2 = f2_pack(c, c), nb2 = f2_pack(nb, nb);
-      uint64_t lsum2 = f2_pack(0.f, 0.f);
+      uint64_t ls[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) ls[i] = f2_pack(0.f, 0.f);
       uint32_t pk[NCOL / 2];
 #pragma unroll
       for (int u = 0; u < NCOL / 2; ++u) {
         float e0, e1;
         f2_unpack(f2_fma(f2_pack(x[2 * u], x[2 * u + 1]), c2, nb2), e0, e1);
         const float p0 = ex2(e0), p1 = ex2(e1);
-        lsum2 = f2_add(lsum2, f2_pack(p0, p1));
+        ls[u & 3] = f2_add(ls[u & 3], f2_pack(p0, p1));
         const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
         pk[u] = *reinterpret_cast<const uint32_t*>(&b);
       }
       {
         float a0, a1;
-        f2_unpack(lsum2, a0, a1);
+        f2_unpack(f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3])), a0, a1);
         l += a0 + a1;  // unrounded weights normalise O and give the LSE
       }
 
