@@ -11,6 +11,10 @@ synchronize.  ``value`` is microseconds per call for the whole job.
 --impl reference times the CPU oracle (the only other implementation of this
 path) on the host cores on a bounded row sample of the same workload and
 extrapolates to microseconds per call.
+
+--op mask / --op accept time the tree steps around verify attention instead
+(the custom_mask build from parent arrays, and the greedy acceptance walk) on
+the trees of the named workload; the default, --op verify, is the attention.
 """
 from __future__ import annotations
 
@@ -324,6 +328,129 @@ def run_ours(args):
     return 0
 
 
+def tree_shapes(name):
+    """(prefix lengths, parent arrays) of a named workload; the Stress trees are
+    drawn directly (seed 5005) so that its 2.5 GB pool is not generated."""
+    if name == "stress":
+        g = torch.Generator().manual_seed(5005)
+        return [131072] * 16, [W.random_parents(64, g) for _ in range(16)], "stress_bs16_p131072_n64"
+    wl = make_workload(name)
+    return wl.prefix_lens, wl.parents, wl.name
+
+
+def run_tree_op(args):
+    ws, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    prefix, trees, wname = tree_shapes(args.workload)
+    bs, sizes = len(trees), [len(t) for t in trees]
+    max_q = max(sizes + [0])
+    total = sum(sizes)
+    g = torch.Generator().manual_seed(77)
+    host = {
+        "parents": torch.tensor([p for t in trees for p in t], dtype=torch.int32),
+        "qo_indptr": torch.tensor([0] + list(np.cumsum(sizes)), dtype=torch.int64),
+        "kv_indptr": torch.tensor([0] + list(np.cumsum(prefix)), dtype=torch.int32),
+        "draft": torch.randint(0, 4, (total,), generator=g, dtype=torch.int32),
+        "target": torch.randint(0, 4, (total,), generator=g, dtype=torch.int32),
+        "root": torch.randint(0, 4, (bs,), generator=g, dtype=torch.int32),
+        "slots": torch.randperm(4 * total + 1, generator=g)[:total].to(torch.int64),
+    }
+    d = {k: v.to(dev) for k, v in host.items()}
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    if args.op == "mask":
+        mask_bytes = sum(n * (p + n) for p, n in zip(prefix, sizes))
+        outs = {"mask": torch.empty(mask_bytes, dtype=torch.uint8, device=dev),
+                "indptr": torch.empty(bs + 1, dtype=torch.int64, device=dev)}
+        in_keys = ("parents", "qo_indptr", "kv_indptr")
+
+        def call():
+            binding.tree_mask_build(d["parents"], d["qo_indptr"], d["kv_indptr"], bs, max_q, binding.MASK_FULL_ROW,
+                                    outs["mask"], outs["indptr"], err)
+    else:
+        outs = {"len": torch.empty(bs, dtype=torch.int32, device=dev),
+                "nodes": torch.empty((bs, max_q), dtype=torch.int32, device=dev),
+                "aslots": torch.empty((bs, max_q), dtype=torch.int64, device=dev),
+                "bonus": torch.empty(bs, dtype=torch.int32, device=dev)}
+        in_keys = ("parents", "qo_indptr", "draft", "target", "root", "slots")
+
+        def call():
+            binding.tree_accept(d["parents"], d["draft"], d["target"], d["root"], d["slots"], d["qo_indptr"], bs,
+                                max_q, outs["len"], outs["nodes"], outs["aslots"], outs["bonus"], err)
+    in_bytes = sum(d[k].numel() * d[k].element_size() for k in in_keys)
+    out_bytes = sum(t.numel() * t.element_size() for t in outs.values())
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, "device error word set during warm-up"
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(k & 0xff)
+            starts[k].record(stream)
+            call()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+    ms = float(np.mean([s_.elapsed_time(e) for s_, e in zip(starts, ends)]))
+    # end to end: inputs from pinned host memory, outputs back, copies timed
+    hpin = {k: host[k].pin_memory() for k in in_keys}
+    hout = {k: torch.empty_like(v, device="cpu").pin_memory() for k, v in outs.items()}
+    e_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for k in range(args.steps + 1):
+        if k:
+            e_s[k - 1].record(stream)
+        for kk in in_keys:
+            d[kk].copy_(hpin[kk], non_blocking=True)
+        call()
+        for kk, t in outs.items():
+            hout[kk].copy_(t, non_blocking=True)
+        if k:
+            e_e[k - 1].record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = float(np.mean([s_.elapsed_time(e) for s_, e in zip(e_s, e_e)]))
+    # the oracle on the host, one whole call
+    from oracle import tree_ops as TO
+    t0 = time.perf_counter()
+    if args.op == "mask":
+        TO.tree_mask(trees, prefix, TO.MASK_FULL_ROW)
+    else:
+        hq = host["qo_indptr"].tolist()
+        for r in range(bs):
+            sl = slice(hq[r], hq[r + 1])
+            TO.tree_accept(trees[r], host["draft"][sl].tolist(), host["target"][sl].tolist(), int(host["root"][r]),
+                           host["slots"][sl].tolist())
+    cpu_us = (time.perf_counter() - t0) * 1e6
+    peaks = load_peaks()
+    nbytes = in_bytes + out_bytes
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": f"tree-{args.op} µs/call (1×GB300)", "value": ms * 1e3, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int32/u8", "data": "synthetic",
+        "config": {"workload": wname, "op": args.op, "bs": bs, "prefix": prefix, "tree": sizes,
+                   "l2": "flushed between calls (256 MiB write outside the timed events)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None,
+                     "peak_source": peaks["source"], "algorithmic_bytes": nbytes},
+        "clocks": clk.summary(), "gpu_launches": args.steps,
+        "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": in_bytes,
+                "d2h_bytes_per_step": out_bytes},
+        "cpu_baseline": {"value": cpu_us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "one whole call, single-threaded Python"},
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def wl_tensor(wl, k):
     return getattr(wl, k).contiguous()
 
@@ -374,11 +501,15 @@ def main():
     ap.add_argument("--simt", action="store_true", help="time the SIMT correctness-floor kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--op", choices=["verify", "mask", "accept"], default="verify",
+                    help="verify attention (default) or one of the tree steps around it")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
     if args.impl == "reference":
         return run_reference(args)
+    if args.op != "verify":
+        return run_tree_op(args)
     return run_ours(args)
 
 

@@ -1,0 +1,98 @@
+/*
+ * mla_tree_ops.h -- C ABI of the two tree steps around MLA tree-verify
+ * attention on GB300 (sm_103a): building the visibility mask from the draft
+ * tree, and accepting the verified tree.
+ *
+ * Where the pages define them (page title -- section):
+ *   - the mask is rebuilt from the tree structure rather than reverse-
+ *     engineered from a packed format: "The Glue That Binds" -- "The
+ *     Thinking Process";
+ *   - tree building and tree acceptance are entry points of the same C-ABI
+ *     library as verify attention: "The Glue That Connects" -- "What the
+ *     Edit Actually Does".
+ *
+ * Conventions (as in mla_tree_verify.h): every pointer named "device" is a
+ * CUDA device pointer; buffers are caller-owned; nothing allocates or
+ * synchronises, so both calls may be captured in a CUDA graph; the return
+ * value is MTV_OK (0) or a negative MTV_E* code (nothing is launched then).
+ * `err` (device, may be NULL) is a sticky 32-bit word the kernels OR
+ * MTV_DEVERR_* bits into; data-dependent problems never trap.
+ */
+#ifndef MLA_TREE_OPS_H_
+#define MLA_TREE_OPS_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "mla_tree_verify.h"
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A parent index outside [-1, i-1] for node i (the node is then treated as
+ * hanging off the prefix root). */
+#define MTV_DEVERR_PARENT 0x8
+
+/*
+ * mla_tree_mask_build -- custom_mask + mask_indptr from per-request parent
+ * arrays, in the layout mla_tree_verify_run reads.
+ *
+ * parents        device, int32 [qo_indptr[bs]]: parents[qo_indptr[r] + i] is
+ *                the tree index of node i's parent, or -1 when node i hangs
+ *                off the prefix (its last token).
+ * qo_indptr      device, int64 [bs + 1]: CSR offsets of the tree nodes.
+ * kv_indptr      device, int32 [bs + 1]: prefix lengths p_r (FULL_ROW only;
+ *                may be NULL for TREE_ONLY).
+ * bs, max_q_per_req  host: request count and the largest tree size n_r.
+ * mask_layout    MTV_MASK_FULL_ROW: request r is row-major [n_r, p_r + n_r]
+ *                with the p_r prefix columns set to 1; MTV_MASK_TREE_ONLY:
+ *                [n_r, n_r].  Row i, tree column t is 1 iff t == i or t is an
+ *                ancestor of i.
+ * custom_mask    device, uint8 output of mask_capacity bytes.
+ * mask_indptr    device, int64 [bs + 1] output: start of each request's block.
+ * err            device uint32 or NULL: MTV_DEVERR_PARENT for a bad parent,
+ *                MTV_DEVERR_INDPTR for a decreasing indptr, a tree larger than
+ *                max_q_per_req or a mask that does not fit mask_capacity (the
+ *                request's rows are then not written).
+ */
+int mla_tree_mask_build(const int32_t* parents, const int64_t* qo_indptr, const int32_t* kv_indptr, int bs,
+                        int max_q_per_req, int mask_layout, uint8_t* custom_mask, uint64_t mask_capacity,
+                        int64_t* mask_indptr, uint32_t* err, void* stream);
+
+/*
+ * mla_tree_accept -- greedy acceptance of each request's verified tree.
+ *
+ * Starting at the prefix root, move to the child whose draft token equals the
+ * target model's token predicted at the current node (the lowest-index child
+ * when several match), until no child matches.
+ *
+ * parents            device, int32 [qo_indptr[bs]] (as above).
+ * draft_tokens       device, int32 [qo_indptr[bs]]: the token drafted at node i.
+ * target_tokens      device, int32 [qo_indptr[bs]]: the target model's token
+ *                    predicted after node i (e.g. the argmax of its logits).
+ * target_root_tokens device, int32 [bs]: the target's token predicted after
+ *                    the prefix.
+ * out_cache_loc      device, int64 [qo_indptr[bs]]: KV slot of every node.
+ * qo_indptr          device, int64 [bs + 1].
+ * accept_len         device, int32 [bs] output: accepted node count.
+ * accept_nodes       device, int32 [bs, max_q_per_req] output: accepted tree
+ *                    indices in path order, -1 after the last.
+ * accept_slots       device, int64 [bs, max_q_per_req] output: their KV slots
+ *                    (the compaction list), -1 after the last.
+ * bonus_tokens       device, int32 [bs] output: the target's prediction after
+ *                    the last accepted node (after the prefix if none).
+ * err                device uint32 or NULL: MTV_DEVERR_PARENT /
+ *                    MTV_DEVERR_INDPTR as above (an oversized tree accepts
+ *                    nothing).
+ */
+int mla_tree_accept(const int32_t* parents, const int32_t* draft_tokens, const int32_t* target_tokens,
+                    const int32_t* target_root_tokens, const int64_t* out_cache_loc, const int64_t* qo_indptr,
+                    int bs, int max_q_per_req, int32_t* accept_len, int32_t* accept_nodes,
+                    int64_t* accept_slots, int32_t* bonus_tokens, uint32_t* err, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MLA_TREE_OPS_H_ */

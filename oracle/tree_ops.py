@@ -1,0 +1,87 @@
+"""CPU oracle for the two tree steps around verify attention -- test infrastructure.
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU legs may
+import this module.  Plain Python loops over small trees; it shares no code
+with the CUDA library.
+
+* ``tree_mask``: the draft tree's visibility mask rebuilt from its parent
+  array ("The Glue That Binds" -- "The Thinking Process": the mask is rebuilt
+  from the tree structure instead of reverse-engineering a packed format;
+  "The Glue That Connects" -- "What the Edit Actually Does": tree building is
+  one of the library's entry points).  Tree token i sees token t iff t is i or
+  an ancestor of i; in the full-row layout every prefix column is set.
+* ``tree_accept``: greedy acceptance of the verified tree ("The Glue That
+  Connects" -- "What the Edit Actually Does": tree acceptance is one of the
+  library's entry points).  Starting at the prefix root, the walk moves to the
+  child whose draft token equals the target model's token predicted at the
+  current node (the lowest-index child when several match) until no child
+  matches; the target's prediction at the last accepted node is the bonus
+  token, and the accepted nodes' KV slots, in path order, are the compaction
+  list.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+ROOT = -1
+MASK_FULL_ROW = 0
+MASK_TREE_ONLY = 1
+
+
+def ancestors_or_self(parents, i):
+    """Tree indices on the path from node i up to (not including) the root."""
+    out = []
+    j = i
+    while j != ROOT:
+        out.append(j)
+        j = parents[j]
+    return out
+
+
+def tree_mask(parents_per_req, prefix_lens, layout=MASK_FULL_ROW):
+    """Packed uint8 mask and int64 mask_indptr for all requests.
+
+    FULL_ROW: request r is row-major [n_r, p_r + n_r]; columns [0, p_r) are 1,
+    column p_r + t is 1 iff t is i or an ancestor of i.
+    TREE_ONLY: request r is row-major [n_r, n_r] with the tree columns only.
+    """
+    chunks, indptr = [], [0]
+    for par, p in zip(parents_per_req, prefix_lens):
+        n = len(par)
+        width = (p + n) if layout == MASK_FULL_ROW else n
+        off = p if layout == MASK_FULL_ROW else 0
+        m = np.zeros((n, width), dtype=np.uint8)
+        if layout == MASK_FULL_ROW:
+            m[:, :p] = 1
+        for i in range(n):
+            for t in ancestors_or_self(par, i):
+                m[i, off + t] = 1
+        chunks.append(m.reshape(-1))
+        indptr.append(indptr[-1] + m.size)
+    mask = np.concatenate(chunks) if chunks else np.zeros(0, dtype=np.uint8)
+    return mask, np.array(indptr, dtype=np.int64)
+
+
+def tree_accept(parents, draft_tokens, target_tokens, target_root_token, slots):
+    """Greedy walk of one request's verified tree.
+
+    parents[i]: parent tree index of node i (ROOT for nodes under the prefix);
+    draft_tokens[i]: the drafted token at node i; target_tokens[i]: the target
+    model's token predicted after node i; target_root_token: its prediction
+    after the prefix; slots[i]: KV slot of node i.
+    Returns (accepted node indices in path order, bonus token, their slots).
+    """
+    n = len(parents)
+    cur, want = ROOT, int(target_root_token)
+    path = []
+    while True:
+        nxt = None
+        for c in range(n):  # lowest-index child of `cur` that carries the predicted token
+            if parents[c] == cur and int(draft_tokens[c]) == want:
+                nxt = c
+                break
+        if nxt is None:
+            break
+        path.append(nxt)
+        cur, want = nxt, int(target_tokens[nxt])
+    return path, want, [int(slots[c]) for c in path]

@@ -19,6 +19,7 @@ FLAG_SIMT_FLOOR = 0x1
 DEVERR_SLOT_RANGE = 0x1
 DEVERR_INDPTR = 0x2
 DEVERR_TIMEOUT = 0x4
+DEVERR_PARENT = 0x8
 PLAN_MAGIC = 0x4D545650
 ABI_VERSION = 1
 
@@ -51,7 +52,7 @@ class MtvError(RuntimeError):
 _lib = None
 SYMBOLS = ("mla_tree_verify_plan", "mla_tree_verify_run", "mla_tree_verify_strerror",
            "mla_tree_verify_clear_device_error", "mla_tree_verify_read_device_error",
-           "mla_tree_verify_run_static")
+           "mla_tree_verify_run_static", "mla_tree_mask_build", "mla_tree_accept")
 
 
 def library_path() -> str:
@@ -83,6 +84,10 @@ def load(path: str | None = None):
     lib.mla_tree_verify_run_static.argtypes = [ctypes.POINTER(MtvPlan), P, P, I64, P, P, P, P, P, P,
                                                ctypes.c_float, P, P, P]
     lib.mla_tree_verify_run_static.restype = I32
+    lib.mla_tree_mask_build.argtypes = [P, P, P, I32, I32, I32, P, U64, P, P, P]
+    lib.mla_tree_mask_build.restype = I32
+    lib.mla_tree_accept.argtypes = [P, P, P, P, P, P, I32, I32, P, P, P, P, P, P]
+    lib.mla_tree_accept.restype = I32
     if path == library_path():
         _lib = lib
     return lib
@@ -181,6 +186,39 @@ def read_device_error(workspace, stream=None) -> int:
     if rc != MTV_OK:
         raise MtvError(rc, "mla_tree_verify_read_device_error")
     return int(v.value)
+
+
+def tree_mask_build(parents, qo_indptr, kv_indptr, bs: int, max_q_per_req: int, mask_layout: int,
+                    custom_mask, mask_indptr, err=None, stream=None, check: bool = True) -> int:
+    """Enqueues the custom_mask + mask_indptr build from int32 parent arrays."""
+    cap = custom_mask.numel() if isinstance(custom_mask, torch.Tensor) else 0
+    ip = _ptr(mask_indptr, torch.int64, "mask_indptr")
+    rc = load().mla_tree_mask_build(
+        _ptr(parents, torch.int32, "parents", ip), _ptr(qo_indptr, torch.int64, "qo_indptr"),
+        _ptr(kv_indptr, torch.int32, "kv_indptr") if kv_indptr is not None else None, int(bs),
+        int(max_q_per_req), int(mask_layout), _ptr(custom_mask, torch.uint8, "custom_mask", ip), int(cap), ip,
+        _ptr(err, torch.int32, "err") if err is not None else None, _stream_handle(stream))
+    if check and rc != MTV_OK:
+        raise MtvError(rc, "mla_tree_mask_build")
+    return rc
+
+
+def tree_accept(parents, draft_tokens, target_tokens, target_root_tokens, out_cache_loc, qo_indptr, bs: int,
+                max_q_per_req: int, accept_len, accept_nodes, accept_slots, bonus_tokens, err=None, stream=None,
+                check: bool = True) -> int:
+    """Enqueues the greedy acceptance walk of every request's verified tree."""
+    any_p = _ptr(accept_len, torch.int32, "accept_len")
+    rc = load().mla_tree_accept(
+        _ptr(parents, torch.int32, "parents", any_p), _ptr(draft_tokens, torch.int32, "draft_tokens", any_p),
+        _ptr(target_tokens, torch.int32, "target_tokens", any_p),
+        _ptr(target_root_tokens, torch.int32, "target_root_tokens"),
+        _ptr(out_cache_loc, torch.int64, "out_cache_loc", any_p), _ptr(qo_indptr, torch.int64, "qo_indptr"),
+        int(bs), int(max_q_per_req), any_p, _ptr(accept_nodes, torch.int32, "accept_nodes", any_p),
+        _ptr(accept_slots, torch.int64, "accept_slots", any_p), _ptr(bonus_tokens, torch.int32, "bonus_tokens"),
+        _ptr(err, torch.int32, "err") if err is not None else None, _stream_handle(stream))
+    if check and rc != MTV_OK:
+        raise MtvError(rc, "mla_tree_accept")
+    return rc
 
 
 class MlaTreeVerify:

@@ -1,0 +1,205 @@
+// The two tree steps around verify attention: the visibility mask rebuilt
+// from the draft tree's parent array ("The Glue That Binds" -- "The Thinking
+// Process") and the greedy acceptance of the verified tree ("The Glue That
+// Connects" -- "What the Edit Actually Does": tree building and acceptance
+// sit behind the same C ABI as verify attention).
+#include <stdint.h>
+
+#include "mla_tree_ops.h"
+#include "mtv_internal.cuh"
+
+namespace mtv {
+namespace {
+
+constexpr int kMaskThreads = 256;
+constexpr int kMaxTreeForMask = 32768;  // dynamic shared memory holds one flag per tree node
+
+__device__ __forceinline__ void set_err(uint32_t* err, uint32_t bits) {
+  if (err) atomicOr(err, bits);
+}
+
+// Size in bytes of request r's mask block (0 for a request whose geometry is
+// invalid; that request is flagged by the block that owns its row 0).
+__device__ __forceinline__ int64_t mask_block_bytes(const int64_t* qo_indptr, const int32_t* kv_indptr, int r,
+                                                    int max_q, int layout, bool* ok) {
+  const int64_t n = qo_indptr[r + 1] - qo_indptr[r];
+  const int64_t p = layout == MTV_MASK_FULL_ROW ? int64_t(kv_indptr[r + 1]) - kv_indptr[r] : 0;
+  *ok = n >= 0 && n <= max_q && p >= 0 && qo_indptr[r] >= 0;
+  return *ok ? n * (p + n) : 0;
+}
+
+// Block (i, r) writes row i of request r; block (0, r) also writes
+// mask_indptr[r + 1] (and block (0, 0) mask_indptr[0]).
+__global__ void __launch_bounds__(kMaskThreads) tree_mask_kernel(const int32_t* parents, const int64_t* qo_indptr,
+                                                                 const int32_t* kv_indptr, int bs, int max_q,
+                                                                 int layout, uint8_t* mask, uint64_t capacity,
+                                                                 int64_t* mask_indptr, uint32_t* err) {
+  extern __shared__ unsigned char vis[];  // [max_q]: tree column t visible from row i
+  __shared__ long long part[kMaskThreads / 32];
+  const int i = blockIdx.x, r = blockIdx.y, tid = threadIdx.x;
+
+  // offset of request r = sum of the earlier requests' block sizes
+  long long acc = 0;
+  for (int rr = tid; rr < r; rr += kMaskThreads) {
+    bool ok_rr;
+    acc += mask_block_bytes(qo_indptr, kv_indptr, rr, max_q, layout, &ok_rr);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((tid & 31) == 0) part[tid >> 5] = acc;
+  __syncthreads();
+  long long off = 0;
+#pragma unroll
+  for (int w = 0; w < kMaskThreads / 32; ++w) off += part[w];
+
+  bool ok;
+  const int64_t bytes = mask_block_bytes(qo_indptr, kv_indptr, r, max_q, layout, &ok);
+  const int64_t q0 = qo_indptr[r];
+  const int64_t n = ok ? qo_indptr[r + 1] - q0 : 0;
+  const int64_t p = (ok && layout == MTV_MASK_FULL_ROW) ? int64_t(kv_indptr[r + 1]) - kv_indptr[r] : 0;
+  const bool fits = uint64_t(off) + uint64_t(bytes) <= capacity;
+  if (i == 0 && tid == 0) {
+    if (r == 0) mask_indptr[0] = 0;
+    mask_indptr[r + 1] = off + bytes;
+    if (!ok || !fits) set_err(err, MTV_DEVERR_INDPTR);
+  }
+  if (!ok || !fits || i >= n) return;
+
+  const int64_t width = p + n;  // TREE_ONLY: p == 0
+  uint8_t* row = mask + off + int64_t(i) * width;
+
+  // ancestors-or-self of node i
+  for (int t = tid; t < n; t += kMaskThreads) vis[t] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    int j = i;
+    for (int steps = 0; j >= 0 && steps <= i; ++steps) {
+      vis[j] = 1;
+      const int pj = parents[q0 + j];
+      if (pj < -1 || pj >= j) {  // not a tree: treat node j as hanging off the prefix
+        set_err(err, MTV_DEVERR_PARENT);
+        break;
+      }
+      j = pj;
+    }
+  }
+  __syncthreads();
+
+  // prefix columns: ones, 16-byte stores on the aligned middle part
+  if (p > 0) {
+    const uintptr_t a = reinterpret_cast<uintptr_t>(row), e = a + uintptr_t(p);
+    const uintptr_t a16 = (a + 15) & ~uintptr_t(15), e16 = e & ~uintptr_t(15);
+    if (a16 >= e16) {
+      for (uintptr_t x = a + tid; x < e; x += kMaskThreads) *reinterpret_cast<uint8_t*>(x) = 1;
+    } else {
+      for (uintptr_t x = a + tid; x < a16; x += kMaskThreads) *reinterpret_cast<uint8_t*>(x) = 1;
+      const uint4 ones = make_uint4(0x01010101u, 0x01010101u, 0x01010101u, 0x01010101u);
+      for (uintptr_t x = a16 + 16 * uintptr_t(tid); x < e16; x += 16 * kMaskThreads)
+        *reinterpret_cast<uint4*>(x) = ones;
+      for (uintptr_t x = e16 + tid; x < e; x += kMaskThreads) *reinterpret_cast<uint8_t*>(x) = 1;
+    }
+  }
+  // tree columns
+  for (int t = tid; t < n; t += kMaskThreads) row[p + t] = vis[t];
+}
+
+// One warp per request walks the tree from the prefix root.
+__global__ void __launch_bounds__(128) tree_accept_kernel(const int32_t* parents, const int32_t* draft,
+                                                          const int32_t* target, const int32_t* target_root,
+                                                          const int64_t* out_cache_loc, const int64_t* qo_indptr,
+                                                          int bs, int max_q, int32_t* accept_len,
+                                                          int32_t* accept_nodes, int64_t* accept_slots,
+                                                          int32_t* bonus, uint32_t* err) {
+  const int r = int((int64_t(blockIdx.x) * blockDim.x + threadIdx.x) >> 5);
+  const int lane = threadIdx.x & 31;
+  if (r >= bs) return;
+  const int64_t q0 = qo_indptr[r];
+  int64_t n = qo_indptr[r + 1] - q0;
+  if (n < 0 || n > max_q || q0 < 0) {
+    if (lane == 0) set_err(err, MTV_DEVERR_INDPTR);
+    n = 0;
+  }
+  int32_t* nodes = accept_nodes + int64_t(r) * max_q;
+  int64_t* slots = accept_slots + int64_t(r) * max_q;
+  int cur = -1, want = target_root[r], len = 0;
+  for (;;) {
+    int nxt = -1;
+    for (int64_t b = 0; b < n && nxt < 0; b += 32) {
+      const int64_t c = b + lane;
+      bool m = false;
+      if (c < n) {
+        int pc = parents[q0 + c];
+        if (pc < -1 || pc >= c) {
+          set_err(err, MTV_DEVERR_PARENT);
+          pc = -1;
+        }
+        m = pc == cur && draft[q0 + c] == want;
+      }
+      const unsigned hit = __ballot_sync(0xffffffffu, m);
+      if (hit) nxt = int(b) + __ffs(hit) - 1;  // lowest-index matching child
+    }
+    if (nxt < 0) break;  // children have larger indices than their parents: at most n steps
+    if (lane == 0) {
+      nodes[len] = nxt;
+      slots[len] = out_cache_loc[q0 + nxt];
+    }
+    ++len;
+    cur = nxt;
+    want = target[q0 + nxt];
+  }
+  for (int k = len + lane; k < max_q; k += 32) {
+    nodes[k] = -1;
+    slots[k] = -1;
+  }
+  if (lane == 0) {
+    accept_len[r] = len;
+    bonus[r] = want;
+  }
+}
+
+}  // namespace
+}  // namespace mtv
+
+extern "C" int mla_tree_mask_build(const int32_t* parents, const int64_t* qo_indptr, const int32_t* kv_indptr,
+                                   int bs, int max_q_per_req, int mask_layout, uint8_t* custom_mask,
+                                   uint64_t mask_capacity, int64_t* mask_indptr, uint32_t* err, void* stream) {
+  if (bs < 0 || max_q_per_req < 0) return MTV_E_BAD_ARGUMENT;
+  if (mask_layout != MTV_MASK_FULL_ROW && mask_layout != MTV_MASK_TREE_ONLY) return MTV_E_BAD_ARGUMENT;
+  if (!mask_indptr) return MTV_E_NULL_POINTER;
+  if (max_q_per_req > mtv::kMaxTreeForMask) return MTV_E_UNSUPPORTED;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (bs == 0) {
+    if (cudaMemsetAsync(mask_indptr, 0, sizeof(int64_t), st) != cudaSuccess) {
+      cudaGetLastError();
+      return MTV_E_CUDA;
+    }
+    return MTV_OK;
+  }
+  if (!qo_indptr || (!parents && max_q_per_req > 0) || (!custom_mask && mask_capacity > 0) ||
+      (mask_layout == MTV_MASK_FULL_ROW && !kv_indptr))
+    return MTV_E_NULL_POINTER;
+  const dim3 grid(unsigned(max_q_per_req > 0 ? max_q_per_req : 1), unsigned(bs));
+  mtv::tree_mask_kernel<<<grid, mtv::kMaskThreads, size_t(max_q_per_req > 0 ? max_q_per_req : 1), st>>>(
+      parents, qo_indptr, kv_indptr, bs, max_q_per_req, mask_layout, custom_mask, mask_capacity, mask_indptr, err);
+  return cudaGetLastError() == cudaSuccess ? MTV_OK : MTV_E_CUDA;
+}
+
+extern "C" int mla_tree_accept(const int32_t* parents, const int32_t* draft_tokens, const int32_t* target_tokens,
+                               const int32_t* target_root_tokens, const int64_t* out_cache_loc,
+                               const int64_t* qo_indptr, int bs, int max_q_per_req, int32_t* accept_len,
+                               int32_t* accept_nodes, int64_t* accept_slots, int32_t* bonus_tokens, uint32_t* err,
+                               void* stream) {
+  if (bs < 0 || max_q_per_req < 0) return MTV_E_BAD_ARGUMENT;
+  if (bs == 0) return MTV_OK;
+  if (!qo_indptr || !target_root_tokens || !accept_len || !bonus_tokens) return MTV_E_NULL_POINTER;
+  if (max_q_per_req > 0 &&
+      (!parents || !draft_tokens || !target_tokens || !out_cache_loc || !accept_nodes || !accept_slots))
+    return MTV_E_NULL_POINTER;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const int threads = 128;
+  const unsigned blocks = unsigned((int64_t(bs) * 32 + threads - 1) / threads);
+  mtv::tree_accept_kernel<<<blocks, threads, 0, st>>>(parents, draft_tokens, target_tokens, target_root_tokens,
+                                                      out_cache_loc, qo_indptr, bs, max_q_per_req, accept_len,
+                                                      accept_nodes, accept_slots, bonus_tokens, err);
+  return cudaGetLastError() == cudaSuccess ? MTV_OK : MTV_E_CUDA;
+}

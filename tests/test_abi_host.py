@@ -21,7 +21,7 @@ def declared_functions():
         if h.endswith(".h"):
             txt = open(os.path.join(ROOT, "include", h)).read()
             txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-            names += re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(mla_tree_verify\w*)\s*\(", txt, flags=re.M)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(mla_tree_\w*)\s*\(", txt, flags=re.M)
     return sorted(set(names))
 
 
@@ -105,3 +105,23 @@ def test_run_host_checks(lib):
     assert lib.mla_tree_verify_clear_device_error(None, None) == -1
     v = ctypes.c_uint32()
     assert lib.mla_tree_verify_read_device_error(None, ctypes.byref(v), None) == -1
+
+
+def test_tree_ops_host_checks(lib):
+    fake = ctypes.c_void_p(0x100000)  # never dereferenced: checks fail first
+    # mla_tree_mask_build(parents, qo_indptr, kv_indptr, bs, max_q, layout, mask, cap, mask_indptr, err, stream)
+    assert lib.mla_tree_mask_build(fake, fake, fake, -1, 8, 0, fake, 64, fake, None, None) == -3
+    assert lib.mla_tree_mask_build(fake, fake, fake, 1, -1, 0, fake, 64, fake, None, None) == -3
+    assert lib.mla_tree_mask_build(fake, fake, fake, 1, 8, 7, fake, 64, fake, None, None) == -3
+    assert lib.mla_tree_mask_build(fake, fake, fake, 1, 8, 0, fake, 64, None, None, None) == -1
+    assert lib.mla_tree_mask_build(fake, fake, fake, 1, 1 << 16, 0, fake, 64, fake, None, None) == -2
+    assert lib.mla_tree_mask_build(fake, None, fake, 1, 8, 0, fake, 64, fake, None, None) == -1
+    assert lib.mla_tree_mask_build(fake, fake, None, 1, 8, 0, fake, 64, fake, None, None) == -1  # FULL_ROW needs p
+    # mla_tree_accept(parents, draft, target, root, ocl, qo_indptr, bs, max_q, len, nodes, slots, bonus, err, s)
+    args = [fake] * 6
+    outs = [fake] * 4
+    assert lib.mla_tree_accept(*args, -1, 8, *outs, None, None) == -3
+    assert lib.mla_tree_accept(*args, 1, -2, *outs, None, None) == -3
+    assert lib.mla_tree_accept(*args, 0, 8, *outs, None, None) == 0  # nothing to do, nothing launched
+    assert lib.mla_tree_accept(fake, fake, fake, None, fake, fake, 1, 8, *outs, None, None) == -1
+    assert lib.mla_tree_accept(*args, 1, 8, fake, None, fake, fake, None, None) == -1

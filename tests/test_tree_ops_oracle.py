@@ -1,0 +1,213 @@
+"""Pins of the tree-step oracle (oracle/tree_ops.py) to things other than itself:
+closed forms for chain and star trees, the reflexive-transitive closure of the
+parent relation (Warshall), invariants, brute force over all root paths for
+acceptance, and planted mistakes that each pin must catch."""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import tree_ops as T
+from paged_mla_speculative_tree_gb300 import workloads as W
+
+
+def closure_mask(parents):
+    """[n, n] reflexive-transitive closure of child -> parent (Warshall)."""
+    n = len(parents)
+    a = np.eye(n, dtype=bool)
+    for i, p in enumerate(parents):
+        if p != T.ROOT:
+            a[i, p] = True
+    for k in range(n):
+        a |= a[:, k:k + 1] & a[k:k + 1, :]
+    return a.astype(np.uint8)
+
+
+def tree_part(mask, indptr, prefix_lens, sizes, layout, r):
+    n, p = sizes[r], prefix_lens[r]
+    w = p + n if layout == T.MASK_FULL_ROW else n
+    blk = mask[indptr[r]:indptr[r + 1]].reshape(n, w)
+    return blk[:, (p if layout == T.MASK_FULL_ROW else 0):], blk
+
+
+def random_trees(seed, count, nmax):
+    g = torch.Generator().manual_seed(seed)
+    out = []
+    for _ in range(count):
+        n = int(torch.randint(1, nmax + 1, (1,), generator=g).item())
+        out.append(W.random_parents(n, g))
+    return out
+
+
+# ---------------------------------------------------------------- mask pins
+def mask_pins_hold(build):
+    """Every mask pin, applied to a mask builder with tree_mask's signature."""
+    trees = random_trees(7, 12, 24) + [W.chain_parents(9), W.star_parents(7), [T.ROOT] * 5, [T.ROOT]]
+    prefix = [int(x) for x in np.random.default_rng(3).integers(0, 40, len(trees))]
+    sizes = [len(t) for t in trees]
+    for layout in (T.MASK_FULL_ROW, T.MASK_TREE_ONLY):
+        mask, indptr = build(trees, prefix, layout)
+        widths = [(p + n) if layout == T.MASK_FULL_ROW else n for p, n in zip(prefix, sizes)]
+        if list(np.diff(indptr)) != [n * w for n, w in zip(sizes, widths)]:
+            return False
+        for r, par in enumerate(trees):
+            tp, blk = tree_part(mask, indptr, prefix, sizes, layout, r)
+            if not np.array_equal(tp, closure_mask(par)):
+                return False
+            if layout == T.MASK_FULL_ROW and not np.all(blk[:, :prefix[r]] == 1):
+                return False
+    # closed forms
+    for n in (1, 2, 8, 33):
+        m, _ = build([W.chain_parents(n)], [0], T.MASK_TREE_ONLY)
+        if not np.array_equal(m.reshape(n, n), np.tril(np.ones((n, n), dtype=np.uint8))):
+            return False
+        m, _ = build([W.star_parents(n)], [0], T.MASK_TREE_ONLY)
+        want = np.eye(n, dtype=np.uint8)
+        want[:, 0] = 1
+        if not np.array_equal(m.reshape(n, n), want):
+            return False
+    return True
+
+
+def test_mask_oracle_meets_its_pins():
+    assert mask_pins_hold(T.tree_mask)
+
+
+def test_mask_invariants_on_random_trees():
+    for par in random_trees(11, 20, 40):
+        m, _ = T.tree_mask([par], [0], T.MASK_TREE_ONLY)
+        n = len(par)
+        m = m.reshape(n, n)
+        for i, p in enumerate(par):
+            assert m[i, i] == 1
+            depth = len(T.ancestors_or_self(par, i))
+            assert int(m[i].sum()) == depth
+            if p != T.ROOT:
+                assert np.all(m[i] >= m[p])  # a node sees everything its parent sees
+                assert m[i, p] == 1
+
+
+@pytest.mark.parametrize("mutant", ["no_self", "parent_only", "prefix_zero", "off_by_one_column"])
+def test_mask_pins_catch_planted_mistakes(mutant):
+    def bad(trees, prefix, layout):
+        mask, indptr = T.tree_mask(trees, prefix, layout)
+        mask = mask.copy()
+        for r, par in enumerate(trees):
+            n, p = len(par), prefix[r]
+            w = p + n if layout == T.MASK_FULL_ROW else n
+            off = p if layout == T.MASK_FULL_ROW else 0
+            blk = mask[indptr[r]:indptr[r + 1]].reshape(n, w)
+            for i in range(n):
+                if mutant == "no_self":
+                    blk[i, off + i] = 0
+                elif mutant == "parent_only":  # forgets the grand-ancestors
+                    row = np.zeros(n, dtype=np.uint8)
+                    row[i] = 1
+                    if par[i] != T.ROOT:
+                        row[par[i]] = 1
+                    blk[i, off:] = row
+                elif mutant == "prefix_zero" and layout == T.MASK_FULL_ROW and p > 0:
+                    blk[i, 0] = 0
+                elif mutant == "off_by_one_column" and i + 1 < n:
+                    blk[i, off:] = np.roll(blk[i, off:], 1)
+        return mask, indptr
+
+    assert not mask_pins_hold(bad)
+
+
+# ---------------------------------------------------------------- acceptance pins
+def brute_force_accept(parents, draft, target, root_tok):
+    """Deepest node whose whole root path was predicted token by token (unique
+    when siblings carry distinct draft tokens)."""
+    best = []
+    for v in range(len(parents)):
+        path = list(reversed(T.ancestors_or_self(parents, v)))
+        want, ok = root_tok, True
+        for u in path:
+            if draft[u] != want:
+                ok = False
+                break
+            want = target[u]
+        if ok and len(path) > len(best):
+            best = path
+    bonus = target[best[-1]] if best else root_tok
+    return best, bonus
+
+
+def distinct_sibling_case(seed, n, vocab=5, hit=0.7):
+    rng = np.random.default_rng(seed)
+    g = torch.Generator().manual_seed(seed)
+    par = W.random_parents(n, g)
+    draft = [0] * n
+    used = {}
+    for i, p in enumerate(par):  # distinct tokens among siblings
+        taken = used.setdefault(p, set())
+        choices = [t for t in range(vocab + n) if t not in taken]
+        draft[i] = int(rng.choice(choices))
+        taken.add(draft[i])
+    # the target agrees with some child of each node with probability `hit`
+    children = {}
+    for i, p in enumerate(par):
+        children.setdefault(p, []).append(i)
+    def predict(node):
+        kids = children.get(node, [])
+        if kids and rng.random() < hit:
+            return draft[int(rng.choice(kids))]
+        return int(rng.integers(1000, 2000))
+    target = [predict(i) for i in range(n)]
+    return par, draft, target, predict(T.ROOT)
+
+
+def accept_pins_hold(accept):
+    for seed in range(40):
+        par, draft, target, root_tok = distinct_sibling_case(seed, 1 + seed % 17)
+        slots = [100 + 3 * i for i in range(len(par))]
+        path, bonus, sl = accept(par, draft, target, root_tok, slots)
+        want_path, want_bonus = brute_force_accept(par, draft, target, root_tok)
+        if path != want_path or bonus != want_bonus or sl != [100 + 3 * c for c in want_path]:
+            return False
+    # chain, every draft predicted: the whole chain is accepted
+    n = 6
+    par = W.chain_parents(n)
+    draft = list(range(10, 10 + n))
+    target = draft[1:] + [77]
+    path, bonus, _ = accept(par, draft, target, 10, list(range(n)))
+    if path != list(range(n)) or bonus != 77:
+        return False
+    # first token mispredicted: nothing accepted, bonus = the root prediction
+    path, bonus, _ = accept(par, draft, target, 11, list(range(n)))
+    if path != [] or bonus != 11:
+        return False
+    # duplicate sibling tokens: the lowest-index child wins
+    par = [T.ROOT, T.ROOT, 1, 0]
+    draft = [5, 5, 7, 7]
+    target = [7, 7, 1, 2]
+    path, bonus, _ = accept(par, draft, target, 5, [0, 1, 2, 3])
+    return path == [0, 3] and bonus == 2
+
+
+def test_accept_oracle_meets_its_pins():
+    assert accept_pins_hold(T.tree_accept)
+
+
+@pytest.mark.parametrize("mutant", ["highest_index", "skip_bonus", "wrong_prediction_index", "stop_after_one"])
+def test_accept_pins_catch_planted_mistakes(mutant):
+    def bad(parents, draft, target, root_tok, slots):
+        n = len(parents)
+        cur, want, path = T.ROOT, root_tok, []
+        while True:
+            order = range(n - 1, -1, -1) if mutant == "highest_index" else range(n)
+            nxt = next((c for c in order if parents[c] == cur and draft[c] == want), None)
+            if nxt is None:
+                break
+            path.append(nxt)
+            cur = nxt
+            want = target[parents[nxt]] if (mutant == "wrong_prediction_index" and parents[nxt] != T.ROOT) \
+                else target[nxt]
+            if mutant == "stop_after_one":
+                break
+        bonus = root_tok if mutant == "skip_bonus" else want
+        return path, bonus, [slots[c] for c in path]
+
+    assert not accept_pins_hold(bad)
