@@ -12,9 +12,10 @@ synchronize.  ``value`` is microseconds per call for the whole job.
 path) on the host cores on a bounded row sample of the same workload and
 extrapolates to microseconds per call.
 
---op mask / --op accept time the tree steps around verify attention instead
-(the custom_mask build from parent arrays, and the greedy acceptance walk) on
-the trees of the named workload; the default, --op verify, is the attention.
+--op mask / --op accept / --op defrag time the steps around verify attention
+instead (the custom_mask build from parent arrays, the greedy acceptance walk,
+the copy of each prefix into one contiguous run of slots) on the named
+workload; the default, --op verify, is the attention.
 """
 from __future__ import annotations
 
@@ -342,6 +343,8 @@ def run_tree_op(args):
     ws, rank, local = dist_env()
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
+    if args.op == "defrag":
+        return run_defrag(args, dev, local)
     prefix, trees, wname = tree_shapes(args.workload)
     bs, sizes = len(trees), [len(t) for t in trees]
     max_q = max(sizes + [0])
@@ -451,6 +454,71 @@ def run_tree_op(args):
     return 0
 
 
+def run_defrag(args, dev, local):
+    """Each request's prefix rows copied into one contiguous run of a second
+    pool (run r starts where run r-1 ends) and its indices rewritten."""
+    wl = make_workload(args.workload)
+    src = wl.kv_pool.to(dev)
+    dst = torch.zeros_like(src)
+    idx = wl.kv_indices.to(dev)
+    indptr = wl.kv_indptr.to(dev)
+    base = torch.tensor([0] + list(np.cumsum(wl.prefix_lens))[:-1], dtype=torch.int64, device=dev)
+    out_idx = torch.empty_like(idx)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        binding.kv_defrag(src, dst, idx, indptr, wl.bs, wl.max_prefix, base, out_idx, err)
+
+    rows = int(wl.kv_indptr[-1])
+    nbytes = rows * 1152 * 2 + rows * 8 * 2 + (wl.bs + 1) * 4 + wl.bs * 8
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    for _ in range(args.warmup):
+        flush.fill_(1)
+        call()
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0, "device error word set during warm-up"
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        for k in range(args.steps):
+            flush.fill_(k & 0xff)
+            starts[k].record(stream)
+            call()
+            ends[k].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+    ms = float(np.mean([s_.elapsed_time(e) for s_, e in zip(starts, ends)]))
+    from oracle import tree_ops as TO
+    sample = min(wl.bs, 2)
+    t0 = time.perf_counter()
+    src16 = wl.kv_pool.view(torch.int16).numpy()
+    TO.kv_defrag(src16, src16, wl.kv_indices.numpy(), wl.kv_indptr.numpy()[:sample + 1], base.cpu().numpy()[:sample])
+    cpu_s = time.perf_counter() - t0
+    cpu_us = cpu_s * 1e6 * rows / max(1, int(wl.kv_indptr[sample]))
+    peaks = load_peaks()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    line = {
+        "metric": "kv-defrag µs/call (1×GB300)", "value": ms * 1e3, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 (copy)", "data": "synthetic",
+        "config": {"workload": wl.name, "op": "defrag", "bs": wl.bs, "rows": rows,
+                   "l2": "flushed between calls (256 MiB write outside the timed events)"},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": gbs / peaks["hbm_gbs"], "traffic": None, "peak_source": peaks["source"],
+                     "algorithmic_bytes": nbytes},
+        "clocks": clk.summary(), "gpu_launches": args.steps,
+        "e2e": {"value": ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                "note": "device-resident pools: the call moves KV inside HBM"},
+        "cpu_baseline": {"value": cpu_us, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": f"{sample} request(s) timed, scaled by rows ({cpu_s:.2f} s)"},
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def wl_tensor(wl, k):
     return getattr(wl, k).contiguous()
 
@@ -501,7 +569,7 @@ def main():
     ap.add_argument("--simt", action="store_true", help="time the SIMT correctness-floor kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--op", choices=["verify", "mask", "accept"], default="verify",
+    ap.add_argument("--op", choices=["verify", "mask", "accept", "defrag"], default="verify",
                     help="verify attention (default) or one of the tree steps around it")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -1,7 +1,7 @@
 /*
- * mla_tree_ops.h -- C ABI of the two tree steps around MLA tree-verify
- * attention on GB300 (sm_103a): building the visibility mask from the draft
- * tree, and accepting the verified tree.
+ * mla_tree_ops.h -- C ABI of the steps around MLA tree-verify attention on
+ * GB300 (sm_103a): building the visibility mask from the draft tree,
+ * accepting the verified tree, and defragmenting a request's paged KV.
  *
  * Where the pages define them (page title -- section):
  *   - the mask is rebuilt from the tree structure rather than reverse-
@@ -13,7 +13,7 @@
  *
  * Conventions (as in mla_tree_verify.h): every pointer named "device" is a
  * CUDA device pointer; buffers are caller-owned; nothing allocates or
- * synchronises, so both calls may be captured in a CUDA graph; the return
+ * synchronises, so every call may be captured in a CUDA graph; the return
  * value is MTV_OK (0) or a negative MTV_E* code (nothing is launched then).
  * `err` (device, may be NULL) is a sticky 32-bit word the kernels OR
  * MTV_DEVERR_* bits into; data-dependent problems never trap.
@@ -90,6 +90,34 @@ int mla_tree_accept(const int32_t* parents, const int32_t* draft_tokens, const i
                     const int32_t* target_root_tokens, const int64_t* out_cache_loc, const int64_t* qo_indptr,
                     int bs, int max_q_per_req, int32_t* accept_len, int32_t* accept_nodes,
                     int64_t* accept_slots, int32_t* bonus_tokens, uint32_t* err, void* stream);
+
+/*
+ * mla_kv_defrag -- copy each request's prefix rows into one contiguous run of
+ * slots and rewrite its prefix indices to that run (the pages' plan to
+ * defragment the paged KV for contiguous reads: "The Glue That Connects" --
+ * "The Context" and "The Final Solder Joint" -- "The Mandate: Three
+ * Priorities").
+ *
+ * For request r and prefix key j < p_r (p_r = kv_indptr[r+1] - kv_indptr[r]):
+ *   kv_dst[dst_base[r] + j, :] = kv_src[kv_indices[kv_indptr[r] + j], :]
+ *   kv_indices_out[kv_indptr[r] + j] = dst_base[r] + j
+ *
+ * kv_src, kv_dst  device, bf16 [num_slots, 576] each, 16-byte aligned; they
+ *                 may be the same pool only if no destination slot of this
+ *                 call is also a source slot of it (not checked).
+ * num_slots       rows in both pools (slots are checked against it).
+ * kv_indices      device, int64 [kv_indptr[bs]]; kv_indptr device, int32 [bs+1].
+ * dst_base        device, int64 [bs]: first destination slot of each request.
+ * kv_indices_out  device, int64 [kv_indptr[bs]] (may alias kv_indices).
+ * max_prefix      host: largest p_r (sizes the grid); longer prefixes are
+ *                 flagged MTV_DEVERR_INDPTR and not copied.
+ * err             device uint32 or NULL: MTV_DEVERR_SLOT_RANGE for a source
+ *                 or destination slot outside [0, num_slots) (that row is not
+ *                 copied and its kv_indices_out entry is not written).
+ */
+int mla_kv_defrag(const void* kv_src, void* kv_dst, int64_t num_slots, const int64_t* kv_indices,
+                  const int32_t* kv_indptr, int bs, int64_t max_prefix, const int64_t* dst_base,
+                  int64_t* kv_indices_out, uint32_t* err, void* stream);
 
 #ifdef __cplusplus
 }

@@ -18,6 +18,11 @@ with the CUDA library.
   matches; the target's prediction at the last accepted node is the bonus
   token, and the accepted nodes' KV slots, in path order, are the compaction
   list.
+* ``kv_defrag``: each request's prefix rows copied into one contiguous run of
+  slots and its prefix indices rewritten to that run ("The Final Solder Joint"
+  -- "The Mandate: Three Priorities": defragmentation is the next priority
+  after graph capture; "The Glue That Connects" -- "The Context": the plan
+  that introduces it).  A numpy gather (library primitive) does the copy.
 """
 from __future__ import annotations
 
@@ -85,3 +90,18 @@ def tree_accept(parents, draft_tokens, target_tokens, target_root_token, slots):
         path.append(nxt)
         cur, want = nxt, int(target_tokens[nxt])
     return path, want, [int(slots[c]) for c in path]
+
+
+def kv_defrag(src_pool, dst_pool, kv_indices, kv_indptr, dst_base):
+    """Returns (new destination pool, new kv_indices): for request r and prefix
+    key j, row dst_base[r] + j of the destination takes source row
+    kv_indices[kv_indptr[r] + j], and that index becomes dst_base[r] + j."""
+    out = np.array(dst_pool, copy=True)
+    idx = np.array(kv_indices, dtype=np.int64, copy=True)
+    src = np.asarray(src_pool)
+    for r in range(len(dst_base)):
+        k0, k1 = int(kv_indptr[r]), int(kv_indptr[r + 1])
+        run = np.arange(int(dst_base[r]), int(dst_base[r]) + (k1 - k0), dtype=np.int64)
+        out[run] = src[idx[k0:k1]]
+        idx[k0:k1] = run
+    return out, idx

@@ -52,7 +52,7 @@ class MtvError(RuntimeError):
 _lib = None
 SYMBOLS = ("mla_tree_verify_plan", "mla_tree_verify_run", "mla_tree_verify_strerror",
            "mla_tree_verify_clear_device_error", "mla_tree_verify_read_device_error",
-           "mla_tree_verify_run_static", "mla_tree_mask_build", "mla_tree_accept")
+           "mla_tree_verify_run_static", "mla_tree_mask_build", "mla_tree_accept", "mla_kv_defrag")
 
 
 def library_path() -> str:
@@ -88,6 +88,8 @@ def load(path: str | None = None):
     lib.mla_tree_mask_build.restype = I32
     lib.mla_tree_accept.argtypes = [P, P, P, P, P, P, I32, I32, P, P, P, P, P, P]
     lib.mla_tree_accept.restype = I32
+    lib.mla_kv_defrag.argtypes = [P, P, I64, P, P, I32, I64, P, P, P, P]
+    lib.mla_kv_defrag.restype = I32
     if path == library_path():
         _lib = lib
     return lib
@@ -218,6 +220,21 @@ def tree_accept(parents, draft_tokens, target_tokens, target_root_tokens, out_ca
         _ptr(err, torch.int32, "err") if err is not None else None, _stream_handle(stream))
     if check and rc != MTV_OK:
         raise MtvError(rc, "mla_tree_accept")
+    return rc
+
+
+def kv_defrag(kv_src, kv_dst, kv_indices, kv_indptr, bs: int, max_prefix: int, dst_base, kv_indices_out,
+              err=None, stream=None, check: bool = True) -> int:
+    """Enqueues the copy of each request's prefix rows into one contiguous run
+    of slots starting at dst_base[r], and the rewrite of their indices."""
+    num_slots = kv_src.shape[0] if isinstance(kv_src, torch.Tensor) else 0
+    rc = load().mla_kv_defrag(
+        _ptr(kv_src, torch.bfloat16, "kv_src"), _ptr(kv_dst, torch.bfloat16, "kv_dst"), int(num_slots),
+        _ptr(kv_indices, torch.int64, "kv_indices"), _ptr(kv_indptr, torch.int32, "kv_indptr"), int(bs),
+        int(max_prefix), _ptr(dst_base, torch.int64, "dst_base"), _ptr(kv_indices_out, torch.int64, "kv_indices_out"),
+        _ptr(err, torch.int32, "err") if err is not None else None, _stream_handle(stream))
+    if check and rc != MTV_OK:
+        raise MtvError(rc, "mla_kv_defrag")
     return rc
 
 

@@ -1,8 +1,10 @@
-// The two tree steps around verify attention: the visibility mask rebuilt
-// from the draft tree's parent array ("The Glue That Binds" -- "The Thinking
-// Process") and the greedy acceptance of the verified tree ("The Glue That
+// The steps around verify attention: the visibility mask rebuilt from the
+// draft tree's parent array ("The Glue That Binds" -- "The Thinking
+// Process"), the greedy acceptance of the verified tree ("The Glue That
 // Connects" -- "What the Edit Actually Does": tree building and acceptance
-// sit behind the same C ABI as verify attention).
+// sit behind the same C ABI as verify attention), and the defragmentation of
+// a request's prefix rows into one contiguous run of slots ("The Final Solder
+// Joint" -- "The Mandate: Three Priorities").
 #include <stdint.h>
 
 #include "mla_tree_ops.h"
@@ -157,8 +159,58 @@ __global__ void __launch_bounds__(128) tree_accept_kernel(const int32_t* parents
   }
 }
 
+// Warp w of block (x, r) copies prefix row j = 8x + w of request r: 72
+// 16-byte units of the 1152-byte row, all loads issued before the stores.
+constexpr int kDefragRowsPerBlock = 8;
+constexpr int kRowUnits = kDQK * 2 / 16;  // 72
+
+__global__ void __launch_bounds__(32 * kDefragRowsPerBlock) kv_defrag_kernel(
+    const uint4* __restrict__ src, uint4* __restrict__ dst, int64_t num_slots, const int64_t* kv_indices,
+    const int32_t* kv_indptr, int64_t max_prefix, const int64_t* dst_base, int64_t* kv_indices_out,
+    uint32_t* err) {
+  const int r = blockIdx.y, lane = threadIdx.x & 31;
+  const int64_t j = int64_t(blockIdx.x) * kDefragRowsPerBlock + (threadIdx.x >> 5);
+  const int64_t k0 = kv_indptr[r];
+  const int64_t p = int64_t(kv_indptr[r + 1]) - k0;
+  if (p < 0 || p > max_prefix || k0 < 0) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) set_err(err, MTV_DEVERR_INDPTR);
+    return;
+  }
+  if (j >= p) return;
+  const int64_t s = kv_indices[k0 + j];
+  const int64_t d = dst_base[r] + j;
+  if (s < 0 || s >= num_slots || d < 0 || d >= num_slots) {
+    if (lane == 0) set_err(err, MTV_DEVERR_SLOT_RANGE);
+    return;
+  }
+  const uint4* a = src + s * kRowUnits;
+  uint4* b = dst + d * kRowUnits;
+  uint4 v0 = a[lane], v1 = a[lane + 32], v2 = make_uint4(0u, 0u, 0u, 0u);
+  if (lane + 64 < kRowUnits) v2 = a[lane + 64];
+  b[lane] = v0;
+  b[lane + 32] = v1;
+  if (lane + 64 < kRowUnits) b[lane + 64] = v2;
+  if (lane == 0) kv_indices_out[k0 + j] = d;
+}
+
 }  // namespace
 }  // namespace mtv
+
+extern "C" int mla_kv_defrag(const void* kv_src, void* kv_dst, int64_t num_slots, const int64_t* kv_indices,
+                             const int32_t* kv_indptr, int bs, int64_t max_prefix, const int64_t* dst_base,
+                             int64_t* kv_indices_out, uint32_t* err, void* stream) {
+  if (bs < 0 || max_prefix < 0 || num_slots < 0) return MTV_E_BAD_ARGUMENT;
+  if (bs == 0 || max_prefix == 0) return MTV_OK;
+  if (!kv_src || !kv_dst || !kv_indices || !kv_indptr || !dst_base || !kv_indices_out) return MTV_E_NULL_POINTER;
+  if ((reinterpret_cast<uintptr_t>(kv_src) | reinterpret_cast<uintptr_t>(kv_dst)) & 15) return MTV_E_BAD_ARGUMENT;
+  const int64_t gx = (max_prefix + mtv::kDefragRowsPerBlock - 1) / mtv::kDefragRowsPerBlock;
+  if (gx > 0x7fffffff || bs > 65535) return MTV_E_UNSUPPORTED;
+  const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(bs));
+  mtv::kv_defrag_kernel<<<grid, 32 * mtv::kDefragRowsPerBlock, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(kv_src), static_cast<uint4*>(kv_dst), num_slots, kv_indices, kv_indptr, max_prefix,
+      dst_base, kv_indices_out, err);
+  return cudaGetLastError() == cudaSuccess ? MTV_OK : MTV_E_CUDA;
+}
 
 extern "C" int mla_tree_mask_build(const int32_t* parents, const int64_t* qo_indptr, const int32_t* kv_indptr,
                                    int bs, int max_q_per_req, int mask_layout, uint8_t* custom_mask,

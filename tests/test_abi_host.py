@@ -21,7 +21,7 @@ def declared_functions():
         if h.endswith(".h"):
             txt = open(os.path.join(ROOT, "include", h)).read()
             txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
-            names += re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(mla_tree_\w*)\s*\(", txt, flags=re.M)
+            names += re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(mla_\w*)\s*\(", txt, flags=re.M)
     return sorted(set(names))
 
 
@@ -125,3 +125,15 @@ def test_tree_ops_host_checks(lib):
     assert lib.mla_tree_accept(*args, 0, 8, *outs, None, None) == 0  # nothing to do, nothing launched
     assert lib.mla_tree_accept(fake, fake, fake, None, fake, fake, 1, 8, *outs, None, None) == -1
     assert lib.mla_tree_accept(*args, 1, 8, fake, None, fake, fake, None, None) == -1
+
+
+def test_kv_defrag_host_checks(lib):
+    fake = ctypes.c_void_p(0x100000)
+    odd = ctypes.c_void_p(0x100008)
+    # mla_kv_defrag(src, dst, num_slots, kv_indices, kv_indptr, bs, max_prefix, dst_base, out, err, stream)
+    assert lib.mla_kv_defrag(fake, fake, 10, fake, fake, -1, 8, fake, fake, None, None) == -3
+    assert lib.mla_kv_defrag(fake, fake, 10, fake, fake, 1, -1, fake, fake, None, None) == -3
+    assert lib.mla_kv_defrag(fake, fake, 10, fake, fake, 0, 8, fake, fake, None, None) == 0
+    assert lib.mla_kv_defrag(None, fake, 10, fake, fake, 1, 8, fake, fake, None, None) == -1
+    assert lib.mla_kv_defrag(fake, fake, 10, fake, fake, 1, 8, None, fake, None, None) == -1
+    assert lib.mla_kv_defrag(odd, fake, 10, fake, fake, 1, 8, fake, fake, None, None) == -3

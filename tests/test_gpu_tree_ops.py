@@ -182,3 +182,64 @@ def test_tree_ops_capture_and_replay():
         path, b, _ = T.tree_accept(trees[r], d[qh[r]:qh[r + 1]], t[qh[r]:qh[r + 1]], rt[r],
                                    wl.out_cache_loc[qh[r]:qh[r + 1]].tolist())
         assert int(alen[r]) == len(path) and int(bonus[r]) == b
+
+
+def defrag_on_gpu(src, dst, kv_indices, kv_indptr, dst_base, max_prefix, out_alias=False):
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    idx_out = kv_indices if out_alias else torch.full_like(kv_indices, -7)
+    binding.kv_defrag(src, dst, kv_indices, kv_indptr, len(dst_base), max_prefix, dst_base, idx_out, err)
+    torch.cuda.synchronize()
+    return idx_out, int(err.item())
+
+
+def test_defrag_long_random_bit_exact_and_attention_unchanged():
+    wl = W.WORKLOADS["long_random"]()
+    d = to_device(wl)
+    o_ref, l_ref = run_gpu(wl, dev_tensors=d)
+    dst = torch.zeros_like(d["kv_pool"])
+    base = 1000
+    idx, err = defrag_on_gpu(d["kv_pool"], dst, d["kv_indices"], d["kv_indptr"],
+                             torch.tensor([base], dtype=torch.int64, device="cuda"), wl.max_prefix)
+    assert err == 0
+    src16 = wl.kv_pool.view(torch.int16).numpy()
+    want_pool, want_idx = T.kv_defrag(src16, np.zeros_like(src16), wl.kv_indices.numpy(), wl.kv_indptr.numpy(),
+                                      [base])
+    np.testing.assert_array_equal(idx.cpu().numpy(), want_idx)
+    np.testing.assert_array_equal(dst.view(torch.int16).cpu().numpy(), want_pool)
+    # move the tree tokens right after the prefix run, then verify reads only the new pool
+    p = wl.prefix_lens[0]
+    new_ocl = torch.arange(base + p, base + p + wl.total_q, dtype=torch.int64, device="cuda")
+    dst[new_ocl] = d["kv_pool"][d["out_cache_loc"]]
+    d2 = dict(d, kv_pool=dst, kv_indices=idx, out_cache_loc=new_ocl)
+    o, l = run_gpu(wl, dev_tensors=d2)
+    np.testing.assert_array_equal(o, o_ref)
+    np.testing.assert_array_equal(l, l_ref)
+
+
+def test_defrag_in_place_ragged_batch_and_aliased_indices():
+    g = torch.Generator().manual_seed(31)
+    pool = W.randn_bf16((4096, 576), g).cuda()
+    prefix = [100, 0, 333, 1]
+    slots = torch.randperm(2048, generator=g)[:sum(prefix)].to(torch.int64)  # sources in [0, 2048)
+    indptr = torch.tensor([0] + list(np.cumsum(prefix)), dtype=torch.int32)
+    starts = [2048, 2500, 3000, 3500]  # destinations in the free half
+    before = pool.view(torch.int16).cpu().numpy()
+    idx = slots.clone().cuda()
+    out_idx, err = defrag_on_gpu(pool, pool, idx, indptr.cuda(), torch.tensor(starts, dtype=torch.int64).cuda(),
+                                 max(prefix), out_alias=True)
+    assert err == 0
+    want_pool, want_idx = T.kv_defrag(before, before, slots.numpy(), indptr.numpy(), starts)
+    np.testing.assert_array_equal(out_idx.cpu().numpy(), want_idx)
+    np.testing.assert_array_equal(pool.view(torch.int16).cpu().numpy(), want_pool)
+
+
+def test_defrag_out_of_range_slots_are_flagged():
+    pool = torch.randn(64, 576).to(torch.bfloat16).cuda()
+    dst = torch.zeros_like(pool)
+    idx = torch.tensor([3, 99, 5], dtype=torch.int64, device="cuda")
+    indptr = torch.tensor([0, 3], dtype=torch.int32, device="cuda")
+    out, err = defrag_on_gpu(pool, dst, idx, indptr, torch.tensor([10], dtype=torch.int64, device="cuda"), 3)
+    assert err & binding.DEVERR_SLOT_RANGE
+    o = out.cpu().tolist()
+    assert o[0] == 10 and o[1] == -7 and o[2] == 12  # the bad row keeps its index slot unwritten
+    assert torch.equal(dst[10], pool[3]) and torch.equal(dst[12], pool[5]) and not dst[11].any()

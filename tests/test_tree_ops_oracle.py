@@ -211,3 +211,56 @@ def test_accept_pins_catch_planted_mistakes(mutant):
         return path, bonus, [slots[c] for c in path]
 
     assert not accept_pins_hold(bad)
+
+
+# ---------------------------------------------------------------- defrag pins
+def defrag_pins_hold(defrag):
+    rng = np.random.default_rng(17)
+    slots, width = 400, 6
+    src = rng.integers(0, 1 << 16, (slots, width)).astype(np.uint16)
+    dst0 = rng.integers(0, 1 << 16, (slots, width)).astype(np.uint16)
+    prefix = [30, 0, 55, 7]
+    perm = rng.permutation(slots)
+    kv_indptr = np.array([0] + list(np.cumsum(prefix)))
+    kv_indices = perm[:kv_indptr[-1]].astype(np.int64)
+    dst_base = np.array([10, 60, 100, 300])
+    out, idx = defrag(src, dst0, kv_indices, kv_indptr, dst_base)
+    touched = np.zeros(slots, dtype=bool)
+    for r, p in enumerate(prefix):
+        k0 = kv_indptr[r]
+        run = np.arange(dst_base[r], dst_base[r] + p)
+        if not np.array_equal(idx[k0:k0 + p], run):  # indices become the contiguous run
+            return False
+        for j in range(p):  # each row of the run is the request's j-th prefix row
+            if not np.array_equal(out[dst_base[r] + j], src[kv_indices[k0 + j]]):
+                return False
+        touched[run] = True
+    if not np.array_equal(out[~touched], dst0[~touched]):  # nothing else changes
+        return False
+    # a prefix that already is the run at its base is left as it was (in place)
+    same = src.copy()
+    o2, i2 = defrag(same, same, np.arange(20, 50, dtype=np.int64), np.array([0, 30]), np.array([20]))
+    return np.array_equal(o2, same) and np.array_equal(i2, np.arange(20, 50))
+
+
+def test_defrag_oracle_meets_its_pins():
+    assert defrag_pins_hold(T.kv_defrag)
+
+
+@pytest.mark.parametrize("mutant", ["shifted_run", "indices_not_rewritten", "reversed_rows"])
+def test_defrag_pins_catch_planted_mistakes(mutant):
+    def bad(src, dst, kv_indices, kv_indptr, dst_base):
+        out, idx = T.kv_defrag(src, dst, kv_indices, kv_indptr, dst_base)
+        if mutant == "shifted_run":
+            out, idx = T.kv_defrag(src, dst, kv_indices, kv_indptr, np.asarray(dst_base) + 1)
+        elif mutant == "indices_not_rewritten":
+            idx = np.array(kv_indices, copy=True)
+        else:
+            for r in range(len(dst_base)):
+                k0, k1 = int(kv_indptr[r]), int(kv_indptr[r + 1])
+                if k1 - k0 > 1:
+                    run = np.arange(dst_base[r], dst_base[r] + k1 - k0)
+                    out[run] = out[run[::-1]]
+        return out, idx
+
+    assert not defrag_pins_hold(bad)
