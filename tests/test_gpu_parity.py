@@ -122,3 +122,32 @@ def test_long_contiguous_equals_random_slots(flags):
     oa, la = G.run_gpu(a, flags)
     ob, lb = G.run_gpu(b, flags)
     assert np.array_equal(oa, ob) and np.array_equal(la, lb)
+
+
+@pytest.mark.parametrize("nsplit", [1, 3])
+def test_growing_scores_move_the_reference_every_tile(flags, nsplit):
+    """Scores that grow along the keys by more than the lazy-rescale threshold
+    (2^8) per 64-key tile, driven through the rope dims: the running max moves
+    on every tile, so the O rescale path and the LSE bookkeeping across moves
+    run many times (random data moves it almost only on the first tile)."""
+    g = torch.Generator().manual_seed(4242)
+    wl = W.custom([280, 200], [W.random_parents(6, g), W.chain_parents(3)], 4096, seed=4243)
+    u = torch.randn(64, generator=g).to(torch.bfloat16).float()
+    thr_raw = 8.0 / (wl.scale * 1.4426950408889634)
+    step = 1.1 * thr_raw / float((u * u).sum())  # per 64 keys
+    q = wl.q.float()
+    q[:, :, :512] = 0.05 * torch.randn(q[:, :, :512].shape, generator=g)
+    q[:, :, 512:] = u + 0.05 * torch.randn(q[:, :, 512:].shape, generator=g)
+    wl.q = q.to(torch.bfloat16)
+    pool = wl.kv_pool.float()
+    for r in range(wl.bs):
+        p = wl.prefix_lens[r]
+        slots = torch.cat([wl.kv_indices[int(wl.kv_indptr[r]):int(wl.kv_indptr[r + 1])],
+                           wl.out_cache_loc[int(wl.qo_indptr[r]):int(wl.qo_indptr[r + 1])]])
+        pos = torch.arange(slots.numel(), dtype=torch.float32)
+        pool[slots, :512] = 0.5 * torch.randn((slots.numel(), 512), generator=g)
+        pool[slots, 512:] = (step * pos / 64.0)[:, None] * u[None, :]
+        assert p + 0 <= slots.numel()
+    wl.kv_pool = pool.to(torch.bfloat16)
+    out, lse = G.run_gpu(wl, flags, nsplit=nsplit)
+    G.compare(wl, out, lse, tag=f"growing nsplit={nsplit}")
