@@ -15,7 +15,8 @@ extrapolates to microseconds per call.
 --op mask / --op accept / --op defrag time the steps around verify attention
 instead (the custom_mask build from parent arrays, the greedy acceptance walk,
 the copy of each prefix into one contiguous run of slots) on the named
-workload; the default, --op verify, is the attention.
+workload; --op shared times requests sharing one prefix, per request and
+grouped into one; the default, --op verify, is the attention.
 """
 from __future__ import annotations
 
@@ -345,6 +346,8 @@ def run_tree_op(args):
     dev = torch.device("cuda", local)
     if args.op == "defrag":
         return run_defrag(args, dev, local)
+    if args.op == "shared":
+        return run_shared(args, dev, local)
     prefix, trees, wname = tree_shapes(args.workload)
     bs, sizes = len(trees), [len(t) for t in trees]
     max_q = max(sizes + [0])
@@ -448,6 +451,84 @@ def run_tree_op(args):
                 "d2h_bytes_per_step": out_bytes},
         "cpu_baseline": {"value": cpu_us, "unit": UNIT, "cores": 1, "kind": "oracle",
                          "sample": "one whole call, single-threaded Python"},
+        "wall_s_timed_region": wall,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_shared(args, dev, local):
+    """Requests that share one prefix: verify per request, against the grouped
+    path (merge into one request per group + mask build + verify), both timed
+    as whole calls."""
+    wl = make_workload(args.workload if args.workload.startswith("shared") else "shared_tree3")
+    d = device_inputs(wl, dev)
+    G = 1
+    n_m = wl.total_q
+    par = torch.tensor([p for t in wl.parents for p in t], dtype=torch.int32, device=dev)
+    gi = torch.tensor([0, wl.bs], dtype=torch.int32, device=dev)
+    kvp = torch.empty(G + 1, dtype=torch.int32, device=dev)
+    idx = torch.empty(wl.prefix_lens[0], dtype=torch.int64, device=dev)
+    qop = torch.empty(G + 1, dtype=torch.int64, device=dev)
+    parout = torch.empty_like(par)
+    mask = torch.empty(n_m * (wl.prefix_lens[0] + n_m), dtype=torch.uint8, device=dev)
+    mip = torch.empty(G + 1, dtype=torch.int64, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    out = torch.empty((wl.total_q, 64, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((wl.total_q, 64), dtype=torch.float32, device=dev)
+    per_req = binding.MlaTreeVerify(wl.bs, wl.max_q_per_req, wl.total_q, wl.max_prefix, device=local)
+    grouped = binding.MlaTreeVerify(G, n_m, wl.total_q, wl.max_prefix, device=local)
+
+    def call_per_request():
+        per_req(d["q"], d["kv_pool"], d["kv_indices"], d["kv_indptr"], d["out_cache_loc"], d["qo_indptr"],
+                d["custom_mask"], d["mask_indptr"], wl.scale, out, lse)
+
+    def call_grouped():
+        binding.tree_group_prefix(gi, G, wl.max_prefix, d["kv_indices"], d["kv_indptr"], d["qo_indptr"], par,
+                                  kvp, idx, qop, parout, err)
+        binding.tree_mask_build(parout, qop, kvp, G, n_m, binding.MASK_FULL_ROW, mask, mip, err)
+        grouped(d["q"], d["kv_pool"], idx, kvp, d["out_cache_loc"], qop, mask, mip, wl.scale, out, lse)
+
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def time_it(fn, clk=None):
+        for _ in range(args.warmup):
+            flush.fill_(1)
+            fn()
+        torch.cuda.synchronize()
+        st = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        en = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+        for k in range(args.steps):
+            flush.fill_(k & 0xff)
+            st[k].record(stream)
+            fn()
+            en[k].record(stream)
+        torch.cuda.synchronize()
+        return float(np.mean([a.elapsed_time(b) for a, b in zip(st, en)]))
+
+    ms_per = time_it(call_per_request)
+    with ClockSampler(local) as clk:
+        t_wall = time.perf_counter()
+        ms = time_it(call_grouped)
+        wall = time.perf_counter() - t_wall
+    assert int(err.item()) == 0 and per_req.device_error() == 0 and grouped.device_error() == 0
+    peaks = load_peaks()
+    flops = wl.algorithmic_flops()
+    tf = flops / (ms * 1e-3) / 1e12
+    line = {
+        "metric": "shared-prefix verify µs/call (1×GB300)", "value": ms * 1e3, "unit": UNIT, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "op": "shared", "bs": wl.bs, "prefix": wl.prefix_lens[0],
+                   "tree": wl.tree_sizes[0], "per_request_us": ms_per * 1e3,
+                   "grouped_includes": "group + mask build + verify",
+                   "l2": "flushed between calls (256 MiB write outside the timed events)"},
+        "roofline": {"bound": "tensor", "achieved": tf, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": tf / peaks["bf16_tflops"], "traffic": None, "peak_source": peaks["source"] + " burst"},
+        "clocks": clk.summary(), "gpu_launches": 4 * args.steps,
+        "e2e": {"value": ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0,
+                "note": "inputs device-resident; see --op verify for the host-buffer path"},
         "wall_s_timed_region": wall,
     }
     print(json.dumps(line), flush=True)
@@ -569,7 +650,7 @@ def main():
     ap.add_argument("--simt", action="store_true", help="time the SIMT correctness-floor kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
-    ap.add_argument("--op", choices=["verify", "mask", "accept", "defrag"], default="verify",
+    ap.add_argument("--op", choices=["verify", "mask", "accept", "defrag", "shared"], default="verify",
                     help="verify attention (default) or one of the tree steps around it")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -1,7 +1,8 @@
 /*
  * mla_tree_ops.h -- C ABI of the steps around MLA tree-verify attention on
  * GB300 (sm_103a): building the visibility mask from the draft tree,
- * accepting the verified tree, and defragmenting a request's paged KV.
+ * accepting the verified tree, defragmenting a request's paged KV, and
+ * merging requests that share a prefix.
  *
  * Where the pages define them (page title -- section):
  *   - the mask is rebuilt from the tree structure rather than reverse-
@@ -118,6 +119,41 @@ int mla_tree_accept(const int32_t* parents, const int32_t* draft_tokens, const i
 int mla_kv_defrag(const void* kv_src, void* kv_dst, int64_t num_slots, const int64_t* kv_indices,
                   const int32_t* kv_indptr, int bs, int64_t max_prefix, const int64_t* dst_base,
                   int64_t* kv_indices_out, uint32_t* err, void* stream);
+
+/* A follower request whose prefix differs from its group leader's (its own
+ * prefix is then ignored: the group attends to the leader's). */
+#define MTV_DEVERR_PREFIX 0x10
+
+/*
+ * mla_tree_group_prefix -- merge runs of consecutive requests that share one
+ * prefix into single requests, so that verify attention gathers the shared
+ * prefix once per row block and packs their tree rows into full row blocks.
+ * (Not on the pages: the plainest extension of their per-request layout.)
+ *
+ * Group g holds requests [group_indptr[g], group_indptr[g+1]).  Its merged
+ * request has the first request's prefix, and as its tree the group's trees
+ * side by side: node i of request r becomes node i + (qo_indptr[r] -
+ * qo_indptr[first]) with its parent shifted the same way (-1 stays -1), so no
+ * tree token sees another request's tokens.  Token order is unchanged: q, out,
+ * lse and out_cache_loc are used as they are.  Build the merged mask with
+ * mla_tree_mask_build(parents_out, qo_indptr_out, kv_indptr_out, ...).
+ *
+ * group_indptr     device, int32 [num_groups + 1], non-decreasing from 0.
+ * num_groups       host.
+ * max_group_prefix host: largest leader prefix (sizes the grid); a longer one
+ *                  is flagged MTV_DEVERR_INDPTR and copied as empty.
+ * kv_indices, kv_indptr, qo_indptr, parents   device, the per-request inputs.
+ * kv_indptr_out    device, int32 [num_groups + 1].
+ * kv_indices_out   device, int64 [sum of the leaders' prefix lengths].
+ * qo_indptr_out    device, int64 [num_groups + 1] (qo_indptr at group starts).
+ * parents_out      device, int32 [qo_indptr[last request + 1]].
+ * err              device uint32 or NULL: MTV_DEVERR_PREFIX for a follower
+ *                  whose prefix is not the leader's (length or slots).
+ */
+int mla_tree_group_prefix(const int32_t* group_indptr, int num_groups, int64_t max_group_prefix,
+                          const int64_t* kv_indices, const int32_t* kv_indptr, const int64_t* qo_indptr,
+                          const int32_t* parents, int32_t* kv_indptr_out, int64_t* kv_indices_out,
+                          int64_t* qo_indptr_out, int32_t* parents_out, uint32_t* err, void* stream);
 
 #ifdef __cplusplus
 }

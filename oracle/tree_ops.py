@@ -23,6 +23,9 @@ with the CUDA library.
   -- "The Mandate: Three Priorities": defragmentation is the next priority
   after graph capture; "The Glue That Connects" -- "The Context": the plan
   that introduces it).  A numpy gather (library primitive) does the copy.
+* ``group_prefix``: runs of requests that share one prefix merged into single
+  requests whose tree is the group's trees side by side (not on the pages:
+  the plainest extension of their per-request layout).
 """
 from __future__ import annotations
 
@@ -105,3 +108,30 @@ def kv_defrag(src_pool, dst_pool, kv_indices, kv_indptr, dst_base):
         out[run] = src[idx[k0:k1]]
         idx[k0:k1] = run
     return out, idx
+
+
+def group_prefix(group_indptr, kv_indices, kv_indptr, qo_indptr, parents_flat):
+    """Merged (kv_indptr, kv_indices, qo_indptr, parents, prefix_mismatch) for
+    groups [group_indptr[g], group_indptr[g+1]) of consecutive requests: the
+    group keeps its first request's prefix; node i of request r becomes node
+    i + qo_indptr[r] - qo_indptr[first] with its parent shifted alike."""
+    kv_out, idx_out, qo_out = [0], [], [int(qo_indptr[int(group_indptr[0])])]
+    par_out = list(int(p) for p in parents_flat)
+    mismatch = False
+    for g in range(len(group_indptr) - 1):
+        a, b = int(group_indptr[g]), int(group_indptr[g + 1])
+        if b > a:
+            lead = list(kv_indices[int(kv_indptr[a]):int(kv_indptr[a + 1])])
+            for r in range(a + 1, b):
+                if list(kv_indices[int(kv_indptr[r]):int(kv_indptr[r + 1])]) != lead:
+                    mismatch = True
+            idx_out += [int(x) for x in lead]
+            q0 = int(qo_indptr[a])
+            for r in range(a, b):
+                for t in range(int(qo_indptr[r]), int(qo_indptr[r + 1])):
+                    p = int(parents_flat[t])
+                    par_out[t] = -1 if p < 0 else p + int(qo_indptr[r]) - q0
+        kv_out.append(len(idx_out))
+        qo_out.append(int(qo_indptr[b if b > a else a]))
+    return (np.array(kv_out, dtype=np.int32), np.array(idx_out, dtype=np.int64),
+            np.array(qo_out, dtype=np.int64), np.array(par_out, dtype=np.int32), mismatch)

@@ -20,6 +20,7 @@ DEVERR_SLOT_RANGE = 0x1
 DEVERR_INDPTR = 0x2
 DEVERR_TIMEOUT = 0x4
 DEVERR_PARENT = 0x8
+DEVERR_PREFIX = 0x10
 PLAN_MAGIC = 0x4D545650
 ABI_VERSION = 1
 
@@ -52,7 +53,8 @@ class MtvError(RuntimeError):
 _lib = None
 SYMBOLS = ("mla_tree_verify_plan", "mla_tree_verify_run", "mla_tree_verify_strerror",
            "mla_tree_verify_clear_device_error", "mla_tree_verify_read_device_error",
-           "mla_tree_verify_run_static", "mla_tree_mask_build", "mla_tree_accept", "mla_kv_defrag")
+           "mla_tree_verify_run_static", "mla_tree_mask_build", "mla_tree_accept", "mla_kv_defrag",
+           "mla_tree_group_prefix")
 
 
 def library_path() -> str:
@@ -90,6 +92,8 @@ def load(path: str | None = None):
     lib.mla_tree_accept.restype = I32
     lib.mla_kv_defrag.argtypes = [P, P, I64, P, P, I32, I64, P, P, P, P]
     lib.mla_kv_defrag.restype = I32
+    lib.mla_tree_group_prefix.argtypes = [P, I32, I64, P, P, P, P, P, P, P, P, P, P]
+    lib.mla_tree_group_prefix.restype = I32
     if path == library_path():
         _lib = lib
     return lib
@@ -235,6 +239,22 @@ def kv_defrag(kv_src, kv_dst, kv_indices, kv_indptr, bs: int, max_prefix: int, d
         _ptr(err, torch.int32, "err") if err is not None else None, _stream_handle(stream))
     if check and rc != MTV_OK:
         raise MtvError(rc, "mla_kv_defrag")
+    return rc
+
+
+def tree_group_prefix(group_indptr, num_groups: int, max_group_prefix: int, kv_indices, kv_indptr, qo_indptr,
+                      parents, kv_indptr_out, kv_indices_out, qo_indptr_out, parents_out, err=None, stream=None,
+                      check: bool = True) -> int:
+    """Enqueues the merge of runs of requests sharing a prefix (see the header)."""
+    rc = load().mla_tree_group_prefix(
+        _ptr(group_indptr, torch.int32, "group_indptr"), int(num_groups), int(max_group_prefix),
+        _ptr(kv_indices, torch.int64, "kv_indices"), _ptr(kv_indptr, torch.int32, "kv_indptr"),
+        _ptr(qo_indptr, torch.int64, "qo_indptr"), _ptr(parents, torch.int32, "parents"),
+        _ptr(kv_indptr_out, torch.int32, "kv_indptr_out"), _ptr(kv_indices_out, torch.int64, "kv_indices_out"),
+        _ptr(qo_indptr_out, torch.int64, "qo_indptr_out"), _ptr(parents_out, torch.int32, "parents_out"),
+        _ptr(err, torch.int32, "err") if err is not None else None, _stream_handle(stream))
+    if check and rc != MTV_OK:
+        raise MtvError(rc, "mla_tree_group_prefix")
     return rc
 
 

@@ -4,7 +4,8 @@
 // Connects" -- "What the Edit Actually Does": tree building and acceptance
 // sit behind the same C ABI as verify attention), and the defragmentation of
 // a request's prefix rows into one contiguous run of slots ("The Final Solder
-// Joint" -- "The Mandate: Three Priorities").
+// Joint" -- "The Mandate: Three Priorities"); and the merge of requests that
+// share a prefix into one (not on the pages: the plainest extension).
 #include <stdint.h>
 
 #include "mla_tree_ops.h"
@@ -193,8 +194,97 @@ __global__ void __launch_bounds__(32 * kDefragRowsPerBlock) kv_defrag_kernel(
   if (lane == 0) kv_indices_out[k0 + j] = d;
 }
 
+// Block (g, y) of the grouping kernel: slice y of group g's leader prefix is
+// copied and compared with every follower's; block y == 0 also publishes the
+// group's offsets and remaps the parents of the group's tokens.
+constexpr int kGroupThreads = 256;
+constexpr int kGroupSlices = 16;
+
+__global__ void __launch_bounds__(kGroupThreads) group_prefix_kernel(
+    const int32_t* group_indptr, int num_groups, int64_t max_prefix, const int64_t* kv_indices,
+    const int32_t* kv_indptr, const int64_t* qo_indptr, const int32_t* parents, int32_t* kv_indptr_out,
+    int64_t* kv_indices_out, int64_t* qo_indptr_out, int32_t* parents_out, uint32_t* err) {
+  __shared__ long long part[kGroupThreads / 32];
+  const int g = blockIdx.x, y = blockIdx.y, tid = threadIdx.x;
+  const int r0 = group_indptr[g], r1 = group_indptr[g + 1];
+  auto leader_len = [&](int gg) -> int64_t {
+    const int a = group_indptr[gg], b = group_indptr[gg + 1];
+    if (b <= a) return 0;
+    const int64_t p = int64_t(kv_indptr[a + 1]) - kv_indptr[a];
+    return (p < 0 || p > max_prefix) ? 0 : p;
+  };
+  // output offset of this group's prefix: leaders' lengths of the earlier groups
+  long long acc = 0;
+  for (int gg = tid; gg < g; gg += kGroupThreads) acc += leader_len(gg);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((tid & 31) == 0) part[tid >> 5] = acc;
+  __syncthreads();
+  long long off = 0;
+#pragma unroll
+  for (int w = 0; w < kGroupThreads / 32; ++w) off += part[w];
+  const int64_t p = leader_len(g);
+  if (y == 0 && tid == 0) {
+    if (g == 0) {
+      kv_indptr_out[0] = 0;
+      qo_indptr_out[0] = qo_indptr[r0];
+    }
+    kv_indptr_out[g + 1] = int32_t(off + p);
+    qo_indptr_out[g + 1] = qo_indptr[r1 > r0 ? r1 : r0];
+    if (r1 > r0) {
+      const int64_t p_raw = int64_t(kv_indptr[r0 + 1]) - kv_indptr[r0];
+      if (p_raw < 0 || p_raw > max_prefix) set_err(err, MTV_DEVERR_INDPTR);
+    }
+  }
+  if (r1 <= r0) return;
+  // slice y of the prefix: copy the leader's slots, compare the followers'
+  const int64_t lo = p * y / kGroupSlices, hi = p * (y + 1) / kGroupSlices;
+  const int64_t k_lead = kv_indptr[r0];
+  bool bad = false;
+  for (int64_t j = lo + tid; j < hi; j += kGroupThreads) {
+    const int64_t s = kv_indices[k_lead + j];
+    kv_indices_out[off + j] = s;
+    for (int r = r0 + 1; r < r1; ++r) {
+      const int64_t pr = int64_t(kv_indptr[r + 1]) - kv_indptr[r];
+      if (pr != p) bad = true;  // (only a follower of the same length is read)
+      else if (kv_indices[kv_indptr[r] + j] != s) bad = true;
+    }
+  }
+  if (y == 0 && tid < r1 - r0 - 1) {  // a follower with a different length but no slots compared above
+    const int r = r0 + 1 + tid;
+    if (int64_t(kv_indptr[r + 1]) - kv_indptr[r] != p) bad = true;
+  }
+  if (bad) set_err(err, MTV_DEVERR_PREFIX);
+  // parents of the group's tokens, shifted by each request's offset in the merged tree
+  const int64_t q0 = qo_indptr[r0];
+  for (int r = r0; r < r1; ++r) {
+    const int64_t a = qo_indptr[r], b = qo_indptr[r + 1];
+    const int64_t shift = a - q0;
+    for (int64_t t = a + int64_t(y) * kGroupThreads + tid; t < b; t += int64_t(kGroupSlices) * kGroupThreads) {
+      const int32_t par = parents[t];
+      parents_out[t] = par < 0 ? -1 : int32_t(par + shift);
+    }
+  }
+}
+
 }  // namespace
 }  // namespace mtv
+
+extern "C" int mla_tree_group_prefix(const int32_t* group_indptr, int num_groups, int64_t max_group_prefix,
+                                     const int64_t* kv_indices, const int32_t* kv_indptr, const int64_t* qo_indptr,
+                                     const int32_t* parents, int32_t* kv_indptr_out, int64_t* kv_indices_out,
+                                     int64_t* qo_indptr_out, int32_t* parents_out, uint32_t* err, void* stream) {
+  if (num_groups < 0 || max_group_prefix < 0 || max_group_prefix > INT32_MAX) return MTV_E_BAD_ARGUMENT;
+  if (num_groups == 0) return MTV_OK;
+  if (!group_indptr || !kv_indices || !kv_indptr || !qo_indptr || !parents || !kv_indptr_out || !kv_indices_out ||
+      !qo_indptr_out || !parents_out)
+    return MTV_E_NULL_POINTER;
+  const dim3 grid(static_cast<unsigned>(num_groups), static_cast<unsigned>(mtv::kGroupSlices));
+  mtv::group_prefix_kernel<<<grid, mtv::kGroupThreads, 0, static_cast<cudaStream_t>(stream)>>>(
+      group_indptr, num_groups, max_group_prefix, kv_indices, kv_indptr, qo_indptr, parents, kv_indptr_out,
+      kv_indices_out, qo_indptr_out, parents_out, err);
+  return cudaGetLastError() == cudaSuccess ? MTV_OK : MTV_E_CUDA;
+}
 
 extern "C" int mla_kv_defrag(const void* kv_src, void* kv_dst, int64_t num_slots, const int64_t* kv_indices,
                              const int32_t* kv_indptr, int bs, int64_t max_prefix, const int64_t* dst_base,

@@ -278,6 +278,29 @@ def stress(replay: int = 0, pool: torch.Tensor | None = None, seed: int = 1005,
                           pool.shape[0], g, pool=pool)
 
 
+def shared_prefix(bs: int = 16, prefix: int = 32768, tree: int = 1, num_slots: int = 65536,
+                  seed: int = 1006) -> Workload:
+    """bs requests whose prefixes are the same slots (one shared context), each
+    with its own tree of ``tree`` nodes (random parents), random slot map."""
+    g = torch.Generator().manual_seed(seed)
+    pool = randn_bf16((num_slots, D_QK), g)
+    perm = torch.randperm(num_slots, generator=g, dtype=torch.int64)
+    parents = [random_parents(tree, g) for _ in range(bs)]
+    shared = perm[:prefix]
+    ocl = perm[prefix:prefix + bs * tree]
+    kv_indices = shared.repeat(bs)
+    kv_indptr = torch.tensor([0] + list(_cumsum([prefix] * bs)), dtype=torch.int32)
+    qo_indptr = torch.tensor([0] + list(_cumsum([tree] * bs)), dtype=torch.int64)
+    vis = [ancestors_and_self(par) for par in parents]
+    custom_mask, mask_indptr = pack_mask([prefix] * bs, vis, MASK_FULL_ROW)
+    q = randn_bf16((bs * tree, NUM_HEADS, D_QK), g)
+    return Workload(name=f"shared_bs{bs}_p{prefix}_n{tree}", bs=bs, prefix_lens=[prefix] * bs,
+                    tree_sizes=[tree] * bs, parents=parents, q=q, kv_pool=pool,
+                    kv_indices=kv_indices.contiguous(), kv_indptr=kv_indptr, out_cache_loc=ocl.contiguous(),
+                    qo_indptr=qo_indptr, custom_mask=custom_mask, mask_indptr=mask_indptr,
+                    meta={"shared_prefix": True})
+
+
 def custom(prefix_lens, parents, num_slots, seed, contiguous=False,
            mask_layout=MASK_FULL_ROW, name="custom") -> Workload:
     """Any shape: used by the tests for ragged and degenerate cases."""
@@ -293,4 +316,7 @@ WORKLOADS = {
     "long_random": lambda: long_context(False),
     "mixed": lambda: mixed(),
     "stress": lambda: stress(0),
+    # not one of the five configurations: requests that share one prefix
+    "shared_decode": lambda: shared_prefix(16, 32768, 1),
+    "shared_tree3": lambda: shared_prefix(16, 32768, 3),
 }

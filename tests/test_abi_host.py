@@ -137,3 +137,15 @@ def test_kv_defrag_host_checks(lib):
     assert lib.mla_kv_defrag(None, fake, 10, fake, fake, 1, 8, fake, fake, None, None) == -1
     assert lib.mla_kv_defrag(fake, fake, 10, fake, fake, 1, 8, None, fake, None, None) == -1
     assert lib.mla_kv_defrag(odd, fake, 10, fake, fake, 1, 8, fake, fake, None, None) == -3
+
+
+def test_group_prefix_host_checks(lib):
+    fake = ctypes.c_void_p(0x100000)
+    # mla_tree_group_prefix(group_indptr, G, max_prefix, kv_indices, kv_indptr, qo_indptr, parents,
+    #                       kv_indptr_out, kv_indices_out, qo_indptr_out, parents_out, err, stream)
+    f7 = [fake] * 4
+    assert lib.mla_tree_group_prefix(fake, -1, 8, *f7, *f7, None, None) == -3
+    assert lib.mla_tree_group_prefix(fake, 1, -1, *f7, *f7, None, None) == -3
+    assert lib.mla_tree_group_prefix(fake, 0, 8, *f7, *f7, None, None) == 0
+    assert lib.mla_tree_group_prefix(None, 1, 8, *f7, *f7, None, None) == -1
+    assert lib.mla_tree_group_prefix(fake, 1, 8, *f7, fake, fake, fake, None, None, None) == -1

@@ -6,7 +6,8 @@ import torch
 
 from oracle import tree_ops as T
 from paged_mla_speculative_tree_gb300 import binding, workloads as W
-from tests.gpu_util import run_gpu, to_device
+import oracle
+from tests.gpu_util import compare, run_gpu, to_device
 from tests.test_tree_ops_oracle import distinct_sibling_case, random_trees
 
 pytestmark = pytest.mark.gpu
@@ -243,3 +244,68 @@ def test_defrag_out_of_range_slots_are_flagged():
     o = out.cpu().tolist()
     assert o[0] == 10 and o[1] == -7 and o[2] == 12  # the bad row keeps its index slot unwritten
     assert torch.equal(dst[10], pool[3]) and torch.equal(dst[12], pool[5]) and not dst[11].any()
+
+
+def group_on_gpu(wl, group_indptr):
+    dev = "cuda"
+    gi = torch.tensor(group_indptr, dtype=torch.int32, device=dev)
+    G = len(group_indptr) - 1
+    par = flat_parents(wl.parents).to(dev)
+    kvp = torch.full((G + 1,), -5, dtype=torch.int32, device=dev)
+    lead_total = sum(wl.prefix_lens[group_indptr[g]] for g in range(G) if group_indptr[g + 1] > group_indptr[g])
+    idx = torch.full((max(lead_total, 1),), -5, dtype=torch.int64, device=dev)[:lead_total]
+    qop = torch.full((G + 1,), -5, dtype=torch.int64, device=dev)
+    parout = torch.full_like(par, -9)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    binding.tree_group_prefix(gi, G, max(wl.prefix_lens), wl.kv_indices.to(dev), wl.kv_indptr.to(dev),
+                              wl.qo_indptr.to(dev), par, kvp, idx, qop, parout, err)
+    torch.cuda.synchronize()
+    return kvp, idx, qop, parout, int(err.item())
+
+
+@pytest.mark.parametrize("groups", [[0, 16], [0, 8, 16], [0, 1, 5, 5, 16], list(range(17))])
+def test_group_prefix_matches_oracle(groups):
+    wl = W.WORKLOADS["shared_tree3"]()
+    kvp, idx, qop, par, err = group_on_gpu(wl, groups)
+    want = T.group_prefix(np.array(groups), wl.kv_indices.numpy(), wl.kv_indptr.numpy(), wl.qo_indptr.numpy(),
+                          [p for t in wl.parents for p in t])
+    assert err == 0 and not want[4]
+    np.testing.assert_array_equal(kvp.cpu().numpy(), want[0])
+    np.testing.assert_array_equal(idx.cpu().numpy(), want[1])
+    np.testing.assert_array_equal(qop.cpu().numpy(), want[2])
+    np.testing.assert_array_equal(par.cpu().numpy(), want[3])
+
+
+@pytest.mark.parametrize("name", ["shared_decode", "shared_tree3"])
+def test_grouped_verify_matches_oracle_of_the_original_requests(name):
+    """group -> mask build -> verify on the merged requests, against the
+    oracle on the original (ungrouped) requests."""
+    wl = W.WORKLOADS[name]()
+    kvp, idx, qop, par, err = group_on_gpu(wl, [0, wl.bs])
+    assert err == 0
+    n_merged = wl.total_q
+    width = wl.prefix_lens[0] + n_merged
+    mask = torch.zeros(n_merged * width, dtype=torch.uint8, device="cuda")
+    mip = torch.zeros(2, dtype=torch.int64, device="cuda")
+    merr = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.tree_mask_build(par, qop, kvp, 1, n_merged, binding.MASK_FULL_ROW, mask, mip, merr)
+    torch.cuda.synchronize()
+    assert int(merr.item()) == 0
+    d = to_device(wl)
+    d.update(kv_indices=idx, kv_indptr=kvp, qo_indptr=qop, custom_mask=mask, mask_indptr=mip)
+    merged = W.Workload(name=wl.name + "_merged", bs=1, prefix_lens=[wl.prefix_lens[0]], tree_sizes=[n_merged],
+                        parents=[par.cpu().tolist()], q=wl.q, kv_pool=wl.kv_pool, kv_indices=idx.cpu(),
+                        kv_indptr=kvp.cpu(), out_cache_loc=wl.out_cache_loc, qo_indptr=qop.cpu(),
+                        custom_mask=mask.cpu(), mask_indptr=mip.cpu())
+    out, lse = run_gpu(merged, dev_tensors=d)
+    rows = np.arange(0, wl.total_q * 64, 7)
+    ref = oracle.mla_tree_verify(wl, rows=rows)
+    compare(wl, out, lse, rows=rows, ref=ref, tag=name + " grouped")
+
+
+def test_group_prefix_mismatch_is_flagged():
+    wl = W.custom([30, 30, 31], [[T.ROOT], [T.ROOT, 0], [T.ROOT]], 512, seed=3)  # three different prefixes
+    kvp, idx, qop, par, err = group_on_gpu(wl, [0, 3])
+    assert err & binding.DEVERR_PREFIX
+    np.testing.assert_array_equal(kvp.cpu().numpy(), [0, 30])  # the leader's prefix is used
+    np.testing.assert_array_equal(idx.cpu().numpy(), wl.kv_indices[:30].numpy())

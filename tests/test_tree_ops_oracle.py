@@ -264,3 +264,61 @@ def test_defrag_pins_catch_planted_mistakes(mutant):
         return out, idx
 
     assert not defrag_pins_hold(bad)
+
+
+# ---------------------------------------------------------------- shared-prefix grouping pins
+def merged_workload(wl, group_indptr, grouping=None):
+    import oracle  # noqa: F401  (fp64 attention oracle, used by the callers)
+    grouping = grouping or T.group_prefix
+    par_flat = [p for t in wl.parents for p in t]
+    kvp, idx, qop, par, bad = grouping(group_indptr, wl.kv_indices.numpy(), wl.kv_indptr.numpy(),
+                                       wl.qo_indptr.numpy(), par_flat)
+    G = len(group_indptr) - 1
+    trees = [list(par[qop[g]:qop[g + 1]]) for g in range(G)]
+    prefix = [int(kvp[g + 1] - kvp[g]) for g in range(G)]
+    mask, mip = T.tree_mask(trees, prefix, T.MASK_FULL_ROW)
+    m = W.Workload(name=wl.name + "_merged", bs=G, prefix_lens=prefix, tree_sizes=[len(t) for t in trees],
+                   parents=trees, q=wl.q, kv_pool=wl.kv_pool, kv_indices=torch.from_numpy(idx),
+                   kv_indptr=torch.from_numpy(kvp), out_cache_loc=wl.out_cache_loc,
+                   qo_indptr=torch.from_numpy(qop), custom_mask=torch.from_numpy(mask),
+                   mask_indptr=torch.from_numpy(mip))
+    return m, bad
+
+
+def test_grouping_preserves_the_attention():
+    import oracle
+    g = torch.Generator().manual_seed(8)
+    wl = W.shared_prefix(bs=5, prefix=150, tree=3, num_slots=1024, seed=9)
+    ref_o, ref_l = oracle.mla_tree_verify(wl)
+    for gi in ([0, 5], [0, 2, 5], [0, 1, 2, 3, 4, 5], [0, 3, 3, 5]):
+        m, bad = merged_workload(wl, np.array(gi))
+        assert not bad
+        o, l = oracle.mla_tree_verify(m)
+        assert np.max(np.abs(o - ref_o)) < 1e-9 and np.max(np.abs(l - ref_l)) < 1e-9
+
+
+def test_grouping_identity_and_mismatch():
+    wl = W.shared_prefix(bs=3, prefix=40, tree=2, num_slots=512, seed=10)
+    par_flat = [p for t in wl.parents for p in t]
+    kvp, idx, qop, par, bad = T.group_prefix(np.arange(4), wl.kv_indices.numpy(), wl.kv_indptr.numpy(),
+                                             wl.qo_indptr.numpy(), par_flat)
+    assert not bad and np.array_equal(kvp, wl.kv_indptr.numpy()) and np.array_equal(idx, wl.kv_indices.numpy())
+    assert np.array_equal(qop, wl.qo_indptr.numpy()) and list(par) == par_flat
+    other = W.custom([40, 40], [[T.ROOT], [T.ROOT]], 512, seed=11)  # two different prefixes
+    *_, bad = T.group_prefix(np.array([0, 2]), other.kv_indices.numpy(), other.kv_indptr.numpy(),
+                             other.qo_indptr.numpy(), [-1, -1])
+    assert bad
+
+
+def test_grouping_pin_catches_unshifted_parents():
+    import oracle
+    wl = W.shared_prefix(bs=3, prefix=64, tree=4, num_slots=512, seed=12)
+    ref_o, _ = oracle.mla_tree_verify(wl)
+
+    def bad(group_indptr, kv_indices, kv_indptr, qo_indptr, parents_flat):
+        kvp, idx, qop, par, mis = T.group_prefix(group_indptr, kv_indices, kv_indptr, qo_indptr, parents_flat)
+        return kvp, idx, qop, np.array(parents_flat, dtype=np.int32), mis  # forgets the shift
+
+    m, _ = merged_workload(wl, np.array([0, 3]), grouping=bad)
+    o, _ = oracle.mla_tree_verify(m)
+    assert np.max(np.abs(o - ref_o)) > 1e-3
