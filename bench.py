@@ -630,12 +630,14 @@ def load_traffic(workload_name, plan):
 
 
 def kernel_revision():
+    """Hash of the sources the partial kernel is built from (its .cu, the
+    headers it includes, and the ABI header)."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_mla_speculative_tree_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in ("partial_tc.cu", "tc_ptx.cuh", "mtv_internal.cuh"):
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "mla_tree_verify.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
