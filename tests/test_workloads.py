@@ -67,3 +67,12 @@ def test_tree_only_layout_small():
     wl = W.custom([5, 9], [W.chain_parents(3), W.star_parents(4)], 64, seed=1,
                   mask_layout=W.MASK_TREE_ONLY)
     _check(wl)
+
+
+def test_shared_prefix_generator_shares_the_prefix_slots():
+    wl = W.shared_prefix(bs=4, prefix=50, tree=3, num_slots=512, seed=1)
+    ind = wl.kv_indices.numpy().reshape(4, 50)
+    assert (ind == ind[0]).all()  # one prefix, listed once per request
+    ocl = wl.out_cache_loc.numpy()
+    assert len(set(ocl.tolist())) == ocl.size and not set(ocl.tolist()) & set(ind[0].tolist())
+    assert wl.kv_indptr.tolist() == [0, 50, 100, 150, 200] and wl.qo_indptr.tolist() == [0, 3, 6, 9, 12]
