@@ -24,9 +24,9 @@
 //   3. the softmax warps send their partial S to the peer CTA (each warp
 //      stages its 32 rows in shared memory and issues one bulk copy that
 //      completes bytes on the peer's barrier; double-buffered, one tile
-//      ahead) as 16-bit integers with one power-of-two exponent per 16 values
-//      (block floating point: error <= 2^-15 of the block's largest
-//      magnitude; the distributed-shared-memory link, not the arithmetic, is
+//      ahead) as 16-bit integers with one power-of-two exponent per row and
+//      warp, i.e. per 32 values (block floating point: error <= 2^-14 of the
+//      block's largest magnitude; the distributed-shared-memory link, not the arithmetic, is
 //      what this exchange costs), add the peer's partial to their own exact
 //      one, apply the tree mask (prefix always visible, tree columns from
 //      custom_mask), and run the fp32 online softmax (two warps per TMEM
