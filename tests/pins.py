@@ -10,6 +10,8 @@ None of this is shared with the oracle or with the CUDA path:
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import torch
 
@@ -82,3 +84,49 @@ def sdpa_chain(wl, r: int):
     v = keys[:, :D_LAT].unsqueeze(0).expand(qh.shape[0], -1, -1)
     o = torch.nn.functional.scaled_dot_product_attention(qh, k, v, attn_mask=mask, scale=wl.scale)
     return o.permute(1, 0, 2).reshape(-1, D_LAT).numpy()
+
+
+# ------------------------------------------------------ hand-derived worked example
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "worked_example.json")
+
+
+def worked_example(mask_layout: int = 0):
+    """The worked example of ``tests/golden/worked_example.json`` as a
+    Workload, plus its expected (out, lse) from the closed forms derived there
+    (rows token-major then head; out dims other than 0 and 1 are zero)."""
+    import json
+    import math
+
+    from paged_mla_speculative_tree_gb300 import workloads as W
+    ex = json.load(open(GOLDEN))
+    H, D = 64, 576
+    pool = torch.zeros((ex["num_slots"], D), dtype=torch.float32)
+    for slot, dims in ex["kv_rows"].items():
+        for d, v in dims.items():
+            pool[int(slot), int(d)] = float(v)
+    q = torch.zeros((2, H, D), dtype=torch.float32)
+    q[:, :, 0] = 1.0
+    q[:, :, 512] = torch.tensor([h % 2 for h in range(H)], dtype=torch.float32)
+    rows = ex["mask_full_row"] if mask_layout == W.MASK_FULL_ROW else ex["mask_tree_only"]
+    mask = torch.tensor([b for row in rows for b in row], dtype=torch.uint8)
+    wl = W.Workload(name="worked_example", bs=1, prefix_lens=[2], tree_sizes=[2], parents=[[W.ROOT, 0]],
+                    q=q.to(torch.bfloat16), kv_pool=pool.to(torch.bfloat16),
+                    kv_indices=torch.tensor(ex["kv_indices"], dtype=torch.int64),
+                    kv_indptr=torch.tensor(ex["kv_indptr"], dtype=torch.int32),
+                    out_cache_loc=torch.tensor(ex["out_cache_loc"], dtype=torch.int64),
+                    qo_indptr=torch.tensor(ex["qo_indptr"], dtype=torch.int64),
+                    custom_mask=mask, mask_indptr=torch.tensor([0, mask.numel()], dtype=torch.int64),
+                    mask_layout=mask_layout, scale=ex["scale"])
+    e = math.e
+    z0, z1 = e + 1 + e ** 2, e + 1 + e ** 2 + 1 / e
+    even = [((8 * e + 16 * e ** 2) / z0, (e + 2 + 3 * e ** 2) / z0, math.log(z0)),
+            ((8 * e + 16 * e ** 2 - 8 / e) / z1, (e + 2 + 3 * e ** 2 + 4 / e) / z1, math.log(z1))]
+    odd = [(8.0, 2.0, 1 + math.log(3)), (4.0, 2.5, 1 + math.log(4))]
+    out = np.zeros((2 * H, D_LAT))
+    lse = np.zeros(2 * H)
+    for t in range(2):
+        for h in range(H):
+            o0, o1, l = (odd if h % 2 else even)[t]
+            out[t * H + h, 0], out[t * H + h, 1], lse[t * H + h] = o0, o1, l
+    return wl, out, lse

@@ -11,6 +11,7 @@ import oracle
 from paged_mla_speculative_tree_gb300 import binding
 from paged_mla_speculative_tree_gb300 import workloads as W
 from tests import gpu_util as G
+from tests import pins
 
 pytestmark = pytest.mark.gpu
 
@@ -37,6 +38,14 @@ def test_ragged_batch_every_row(flags, nsplit):
     wl = W.custom([0, 77, 300, 129], parents, 2048, seed=78)
     out, lse = G.run_gpu(wl, flags, nsplit=nsplit)
     G.compare(wl, out, lse, tag=f"ragged nsplit={nsplit}")
+
+
+@pytest.mark.parametrize("layout", [W.MASK_FULL_ROW, W.MASK_TREE_ONLY])
+def test_hand_derived_worked_example(flags, layout):
+    # tests/golden/worked_example.json: outputs in closed form, no oracle involved
+    wl, ref_out, ref_lse = pins.worked_example(layout)
+    out, lse = G.run_gpu(wl, flags)
+    G.compare(wl, out, lse, ref=(ref_out, ref_lse), tag="worked example")
 
 
 def test_tree_only_layout(flags):

@@ -10,6 +10,8 @@
 * closed forms: p=0 and self-only visibility gives out = v_self and
   lse = scale*q.k_self; identical keys give out = v, lse = s + ln(#visible);
 * exhaustive enumeration of every 5-node parent array against the brute force;
+* a hand-derived worked example (tests/golden/worked_example.json) whose
+  outputs are closed forms in e;
 * planted mistakes: copies of the oracle source with one plausible bug each
   must fail at least one pin.
 """
@@ -221,6 +223,23 @@ def test_every_five_node_tree_against_bruteforce():
         check_dense(wl, tag=str(parents))
 
 
+# ---------------------------------------------------------------- hand-derived worked example
+
+@pytest.mark.parametrize("layout", [W.MASK_FULL_ROW, W.MASK_TREE_ONLY])
+def test_hand_derived_worked_example(layout):
+    """tests/golden/worked_example.json: small exact scores, outputs in closed
+    form; pins the mask offset p_r + t, unread prefix columns, the rope dims,
+    the scale and the natural-log LSE on a case checkable by hand."""
+    wl, ref_out, ref_lse = pins.worked_example(layout)
+    out, lse = oracle.mla_tree_verify(wl)
+    np.testing.assert_allclose(lse, ref_lse, rtol=1e-12, atol=1e-12)
+    np.testing.assert_allclose(out, ref_out, rtol=1e-12, atol=1e-12)
+
+
+def test_hand_derived_worked_example_full_row():
+    test_hand_derived_worked_example(W.MASK_FULL_ROW)
+
+
 # ---------------------------------------------------------------- lse combine
 
 def test_lse_combine_equals_unsplit_softmax():
@@ -272,6 +291,7 @@ PIN_FUNCS = [
     test_dense_bruteforce_random_trees, test_dense_bruteforce_degenerate_requests,
     test_chain_equals_sdpa_causal, test_self_only_without_prefix_closed_form,
     test_identical_keys_closed_form, test_lse_combine_equals_unsplit_softmax,
+    test_hand_derived_worked_example_full_row,
 ]
 
 
