@@ -106,7 +106,7 @@ def worked_example(mask_layout: int = 0):
         for d, v in dims.items():
             pool[int(slot), int(d)] = float(v)
     q = torch.zeros((2, H, D), dtype=torch.float32)
-    q[:, :, 0] = 1.0
+    q[:, :, 0] = float(ex["q_dim0"])
     q[:, :, 512] = torch.tensor([h % 2 for h in range(H)], dtype=torch.float32)
     rows = ex["mask_full_row"] if mask_layout == W.MASK_FULL_ROW else ex["mask_tree_only"]
     mask = torch.tensor([b for row in rows for b in row], dtype=torch.uint8)
@@ -120,9 +120,9 @@ def worked_example(mask_layout: int = 0):
                     mask_layout=mask_layout, scale=ex["scale"])
     e = math.e
     z0, z1 = e + 1 + e ** 2, e + 1 + e ** 2 + 1 / e
-    even = [((8 * e + 16 * e ** 2) / z0, (e + 2 + 3 * e ** 2) / z0, math.log(z0)),
-            ((8 * e + 16 * e ** 2 - 8 / e) / z1, (e + 2 + 3 * e ** 2 + 4 / e) / z1, math.log(z1))]
-    odd = [(8.0, 2.0, 1 + math.log(3)), (4.0, 2.5, 1 + math.log(4))]
+    even = [((e / 2 + e ** 2) / z0, (e / 8 + 1 / 4 + 3 * e ** 2 / 8) / z0, math.log(z0)),
+            ((e / 2 + e ** 2 - 1 / (2 * e)) / z1, (e / 8 + 1 / 4 + 3 * e ** 2 / 8 + 1 / (2 * e)) / z1, math.log(z1))]
+    odd = [(0.5, 0.25, 1 + math.log(3)), (0.25, 0.3125, 1 + math.log(4))]
     out = np.zeros((2 * H, D_LAT))
     lse = np.zeros(2 * H)
     for t in range(2):
