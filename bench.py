@@ -74,8 +74,10 @@ def dist_env():
 
 
 class ClockSampler:
-    """SM clock and clock-event reasons sampled every ~2 ms during the timed
-    region through NVML (ctypes; read-only queries), else nvidia-smi."""
+    """SM clock and clock-event reasons sampled during the timed region through
+    NVML (ctypes; read-only queries): a background thread every ~0.5 ms, plus
+    synchronous samples the timed loop takes between launches (``sample()``),
+    so that even a region of a few milliseconds is sampled under load."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
@@ -114,16 +116,22 @@ class ClockSampler:
         except Exception as e:  # pragma: no cover - depends on the box
             self.err = str(e)
 
-    def _poll(self):
+    def sample(self):
+        """One synchronous clock + reasons sample (no-op without NVML)."""
+        if self.nvml is None:
+            return
         import ctypes
         mhz = ctypes.c_uint()
         rs = ctypes.c_ulonglong()
+        if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
+            self.samples.append(float(mhz.value))
+        if self._reason_fn(self.handle, ctypes.byref(rs)) == 0:
+            self.reasons |= int(rs.value)
+
+    def _poll(self):
         while not self._stop.is_set():
-            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(mhz)) == 0:
-                self.samples.append(float(mhz.value))
-            if self._reason_fn(self.handle, ctypes.byref(rs)) == 0:
-                self.reasons |= int(rs.value)
-            time.sleep(0.002)
+            self.sample()
+            time.sleep(0.0005)
 
     def __enter__(self):
         if self.nvml is not None:
@@ -281,6 +289,8 @@ def run_ours(args):
             starts[k].record(stream)
             call()
             ends[k].record(stream)
+            if k % 2 == 1:
+                clk.sample()  # host-side, between launches: the GPU is still busy with the queued steps
         torch.cuda.synchronize()
         if ws > 1:
             torch.distributed.barrier()
@@ -423,6 +433,8 @@ def run_tree_op(args):
             starts[k].record(stream)
             call()
             ends[k].record(stream)
+            if k % 2 == 1:
+                clk.sample()
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall
     ms = float(np.mean([s_.elapsed_time(e) for s_, e in zip(starts, ends)]))
@@ -589,6 +601,8 @@ def run_defrag(args, dev, local):
             starts[k].record(stream)
             call()
             ends[k].record(stream)
+            if k % 2 == 1:
+                clk.sample()
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall
     ms = float(np.mean([s_.elapsed_time(e) for s_, e in zip(starts, ends)]))
