@@ -8,7 +8,7 @@ from oracle import tree_ops as T
 from paged_mla_speculative_tree_gb300 import binding, workloads as W
 import oracle
 from tests.gpu_util import compare, run_gpu, to_device
-from tests.test_tree_ops_oracle import distinct_sibling_case, random_trees
+from tests.test_tree_ops_oracle import distinct_sibling_case, flat_golden_mask, random_trees, tree_steps_example
 
 pytestmark = pytest.mark.gpu
 
@@ -139,6 +139,37 @@ def test_accept_matches_oracle():
         assert list(nodes[r, :len(path)]) == path and np.all(nodes[r, len(path):] == -1)
         assert list(aslots[r, :len(path)]) == sl and np.all(aslots[r, len(path):] == -1)
         assert bonus[r] == b
+
+
+@pytest.mark.parametrize("layout", [T.MASK_FULL_ROW, T.MASK_TREE_ONLY])
+def test_tree_steps_hand_derived_example(layout):
+    # tests/golden/tree_steps_example.json: mask rows and the acceptance walk derived by hand
+    ex = tree_steps_example()
+    mask, indptr, err = build_on_gpu(ex["parents"], ex["prefix_lens"], layout)
+    want, want_ip = flat_golden_mask(ex["mask_full_row" if layout == T.MASK_FULL_ROW else "mask_tree_only"])
+    assert err == 0
+    np.testing.assert_array_equal(indptr, want_ip)
+    np.testing.assert_array_equal(mask, want)
+    bs, max_q = len(ex["parents"]), max(len(p) for p in ex["parents"])
+    flat = lambda key, dt: torch.tensor([v for per in ex[key] for v in per], dtype=dt).cuda()
+    sizes = [len(p) for p in ex["parents"]]
+    qo = torch.tensor([0] + list(np.cumsum(sizes)), dtype=torch.int64).cuda()
+    alen = torch.full((bs,), -9, dtype=torch.int32, device="cuda")
+    nodes = torch.full((bs, max_q), -9, dtype=torch.int32, device="cuda")
+    aslots = torch.full((bs, max_q), -9, dtype=torch.int64, device="cuda")
+    bonus = torch.full((bs,), -9, dtype=torch.int32, device="cuda")
+    aerr = torch.zeros(1, dtype=torch.int32, device="cuda")
+    binding.tree_accept(flat("parents", torch.int32), flat("draft_tokens", torch.int32),
+                        flat("target_tokens", torch.int32),
+                        torch.tensor(ex["target_root_tokens"], dtype=torch.int32).cuda(),
+                        flat("out_cache_loc", torch.int64), qo, bs, max_q, alen, nodes, aslots, bonus, aerr)
+    torch.cuda.synchronize()
+    assert int(aerr.item()) == 0
+    for r, exp in enumerate(ex["expected_accept"]):
+        k = len(exp["nodes"])
+        assert int(alen[r]) == k and int(bonus[r]) == exp["bonus"]
+        assert nodes[r, :k].tolist() == exp["nodes"] and aslots[r, :k].tolist() == exp["slots"]
+        assert bool((nodes[r, k:] == -1).all()) and bool((aslots[r, k:] == -1).all())
 
 
 def test_tree_ops_capture_and_replay():

@@ -1,7 +1,8 @@
 """Pins of the tree-step oracle (oracle/tree_ops.py) to things other than itself:
 closed forms for chain and star trees, the reflexive-transitive closure of the
 parent relation (Warshall), invariants, brute force over all root paths for
-acceptance, and planted mistakes that each pin must catch."""
+acceptance, a hand-derived worked example (tests/golden/tree_steps_example.json)
+and planted mistakes that each pin must catch."""
 import itertools
 
 import numpy as np
@@ -31,6 +32,20 @@ def tree_part(mask, indptr, prefix_lens, sizes, layout, r):
     return blk[:, (p if layout == T.MASK_FULL_ROW else 0):], blk
 
 
+def tree_steps_example():
+    """tests/golden/tree_steps_example.json (visibility and the acceptance walk derived by hand)."""
+    import json
+    import os
+    return json.load(open(os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden",
+                                       "tree_steps_example.json")))
+
+
+def flat_golden_mask(rows_per_req):
+    mask = np.array([b for rows in rows_per_req for row in rows for b in row], dtype=np.uint8)
+    indptr = np.cumsum([0] + [len(rows) * len(rows[0]) for rows in rows_per_req]).astype(np.int64)
+    return mask, indptr
+
+
 def random_trees(seed, count, nmax):
     g = torch.Generator().manual_seed(seed)
     out = []
@@ -43,6 +58,12 @@ def random_trees(seed, count, nmax):
 # ---------------------------------------------------------------- mask pins
 def mask_pins_hold(build):
     """Every mask pin, applied to a mask builder with tree_mask's signature."""
+    ex = tree_steps_example()  # hand-derived rows
+    for layout, key in ((T.MASK_FULL_ROW, "mask_full_row"), (T.MASK_TREE_ONLY, "mask_tree_only")):
+        want, want_ip = flat_golden_mask(ex[key])
+        got, got_ip = build(ex["parents"], ex["prefix_lens"], layout)
+        if not (np.array_equal(got, want) and np.array_equal(got_ip, want_ip)):
+            return False
     trees = random_trees(7, 12, 24) + [W.chain_parents(9), W.star_parents(7), [T.ROOT] * 5, [T.ROOT]]
     prefix = [int(x) for x in np.random.default_rng(3).integers(0, 40, len(trees))]
     sizes = [len(t) for t in trees]
@@ -160,6 +181,12 @@ def distinct_sibling_case(seed, n, vocab=5, hit=0.7):
 
 
 def accept_pins_hold(accept):
+    ex = tree_steps_example()  # hand-derived walk
+    for r, exp in enumerate(ex["expected_accept"]):
+        got = accept(ex["parents"][r], ex["draft_tokens"][r], ex["target_tokens"][r], ex["target_root_tokens"][r],
+                     ex["out_cache_loc"][r])
+        if list(got[0]) != exp["nodes"] or got[1] != exp["bonus"] or list(got[2]) != exp["slots"]:
+            return False
     for seed in range(40):
         par, draft, target, root_tok = distinct_sibling_case(seed, 1 + seed % 17)
         slots = [100 + 3 * i for i in range(len(par))]
@@ -322,3 +349,20 @@ def test_grouping_pin_catches_unshifted_parents():
     m, _ = merged_workload(wl, np.array([0, 3]), grouping=bad)
     o, _ = oracle.mla_tree_verify(m)
     assert np.max(np.abs(o - ref_o)) > 1e-3
+
+
+@pytest.mark.parametrize("layout", [T.MASK_FULL_ROW, T.MASK_TREE_ONLY])
+def test_mask_oracle_matches_hand_derived_example(layout):
+    ex = tree_steps_example()
+    want, want_ip = flat_golden_mask(ex["mask_full_row" if layout == T.MASK_FULL_ROW else "mask_tree_only"])
+    got, got_ip = T.tree_mask(ex["parents"], ex["prefix_lens"], layout)
+    np.testing.assert_array_equal(got_ip, want_ip)
+    np.testing.assert_array_equal(got, want)
+
+
+def test_accept_oracle_matches_hand_derived_example():
+    ex = tree_steps_example()
+    for r, exp in enumerate(ex["expected_accept"]):
+        path, bonus, slots = T.tree_accept(ex["parents"][r], ex["draft_tokens"][r], ex["target_tokens"][r],
+                                           ex["target_root_tokens"][r], ex["out_cache_loc"][r])
+        assert path == exp["nodes"] and bonus == exp["bonus"] and slots == exp["slots"]
