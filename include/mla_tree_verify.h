@@ -68,16 +68,23 @@ extern "C" {
 /* ------------------------------------------------------------ plan flags */
 /* Use the SIMT fp32 correctness-floor kernel instead of the tcgen05 one.     */
 #define MTV_FLAG_SIMT_FLOOR 0x1
+/* Test only: every pipeline wait of the kernels gives up as soon as it has to
+ * spin, so that the timeout path (MTV_DEVERR_TIMEOUT, orderly wind-down, the
+ * call still returns) can be exercised without a fault.  Results of a run with
+ * this flag are undefined; never set it in production.                       */
+#define MTV_FLAG_TEST_SHORT_WAITS 0x100
 
 /* ------------------------------------------------ device error word bits */
 /* The first 4 bytes of the workspace hold a sticky error word that kernels OR
  * into.  Offending keys are treated as masked; nothing traps.                */
 #define MTV_DEVERR_SLOT_RANGE 0x1     /* a slot index outside [0, num_slots)          */
-#define MTV_DEVERR_INDPTR 0x2         /* decreasing indptr or a request beyond the plan's bounds */
+#define MTV_DEVERR_INDPTR 0x2         /* decreasing indptr, a request beyond the plan's bounds,
+                                         or CSR offsets past the end of kv_indices,
+                                         out_cache_loc or custom_mask (see run)  */
 #define MTV_DEVERR_TIMEOUT 0x4        /* a bounded pipeline wait gave up              */
 
 #define MTV_PLAN_MAGIC 0x4D545650u    /* 'MTVP' */
-#define MTV_ABI_VERSION 1u
+#define MTV_ABI_VERSION 2u
 
 /* POD plan.  Produced on the host by mla_tree_verify_plan from upper bounds
  * only (never from device data), then passed unchanged to every run.  The
@@ -110,7 +117,7 @@ typedef struct mtv_plan {
  * max_prefix     largest prefix p_r a run may present.
  * num_heads / d_latent / d_rope   must be 64 / 512 / 64.
  * mask_layout    MTV_MASK_FULL_ROW or MTV_MASK_TREE_ONLY.
- * flags          0 or MTV_FLAG_SIMT_FLOOR.
+ * flags          0, MTV_FLAG_SIMT_FLOOR and/or MTV_FLAG_TEST_SHORT_WAITS.
  * nsplit_override 0 = automatic, else the split count to use (tuning).
  * plan_out       host memory, filled on success.
  * ws_bytes_out   host memory (may be NULL), receives plan_out->ws_bytes.
@@ -129,13 +136,18 @@ int mla_tree_verify_plan(int device, int bs, int max_q_per_req, int64_t total_q_
  * q              device, bf16 [total_q, 64, 576] row-major (token, head, dim).
  * kv_pool        device, bf16 [num_slots, 576], 16-byte aligned; V is columns
  *                0..511 of each row.
- * num_slots      rows in kv_pool, 0 <= num_slots < 2^31 (slot indices are
- *                checked against it; an out-of-range slot is treated as masked).
- * kv_indices     device, int64 [kv_indptr[bs]]: prefix slots, request-major.
+ * num_slots      rows in kv_pool, 0 <= num_slots < 2^31 (the gather keeps a
+ *                slot in a 32-bit register; slot indices are checked against
+ *                num_slots and an out-of-range slot is treated as masked).
+ * kv_indices     device, int64 [kv_indices_len]: prefix slots, request-major.
+ * kv_indices_len number of int64 elements readable at kv_indices (>= 0).
  * kv_indptr      device, int32 [bs + 1]: CSR offsets into kv_indices.
- * out_cache_loc  device, int64 [qo_indptr[bs]]: slot of every tree token.
+ * out_cache_loc  device, int64 [out_cache_loc_len]: slot of every tree token.
+ * out_cache_loc_len  number of int64 elements readable at out_cache_loc.
  * qo_indptr      device, int64 [bs + 1]: CSR offsets of tree tokens (rows of q).
- * custom_mask    device, uint8: per-request visibility (see MTV_MASK_*).
+ * custom_mask    device, uint8 [custom_mask_len]: per-request visibility
+ *                (see MTV_MASK_*).
+ * custom_mask_len  number of bytes readable at custom_mask.
  * mask_indptr    device, int64 [bs + 1]: start of request r's mask block.
  * scale          softmax scale applied to q.k (e.g. 192^-0.5).
  * out            device, bf16 [total_q, 64, 512]; rows past qo_indptr[bs] untouched.
@@ -145,18 +157,26 @@ int mla_tree_verify_plan(int device, int bs, int max_q_per_req, int64_t total_q_
  *                mla_tree_verify_clear_device_error before the first run).
  * stream         a cudaStream_t passed as void* (NULL = legacy default stream).
  *
- * Sizes of each request come from the device buffers and must respect the
- * plan's bounds (n_r <= max_q_per_req, p_r <= max_prefix, qo_indptr[bs] <=
- * total_q_max); violations set MTV_DEVERR_INDPTR and the request is skipped.
+ * Sizes of each request come from the device buffers ("The Final Solder
+ * Joint" -- "The Three-Edits Sequence": everything is derived on the device
+ * from the native buffers) and are checked there before any of them is used
+ * as an offset: n_r <= max_q_per_req, p_r <= max_prefix, kv_indptr and
+ * qo_indptr non-decreasing from >= 0, qo_indptr[r+1] <= min(total_q_max,
+ * out_cache_loc_len), kv_indptr[r+1] <= kv_indices_len, and request r's mask
+ * block (n_r x (p_r + n_r) bytes for FULL_ROW, n_r x n_r for TREE_ONLY) inside
+ * [0, custom_mask_len).  A request failing any check sets MTV_DEVERR_INDPTR and
+ * is skipped: none of its offsets is dereferenced and its rows of out/lse are
+ * left untouched.
  * A row with no visible key gets out = 0 and lse = -inf.
  * No host sync, no allocation: safe to capture in a CUDA graph.
  */
 int mla_tree_verify_run(const mtv_plan_t* plan, const void* q, const void* kv_pool,
-                        int64_t num_slots, const int64_t* kv_indices, const int32_t* kv_indptr,
-                        const int64_t* out_cache_loc, const int64_t* qo_indptr,
-                        const uint8_t* custom_mask, const int64_t* mask_indptr, float scale,
-                        void* out, float* lse, void* workspace, uint64_t workspace_bytes,
-                        void* stream);
+                        int64_t num_slots, const int64_t* kv_indices, int64_t kv_indices_len,
+                        const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                        int64_t out_cache_loc_len, const int64_t* qo_indptr,
+                        const uint8_t* custom_mask, int64_t custom_mask_len,
+                        const int64_t* mask_indptr, float scale, void* out, float* lse,
+                        void* workspace, uint64_t workspace_bytes, void* stream);
 
 /* Text for a return code (static storage; never NULL). */
 const char* mla_tree_verify_strerror(int code);
@@ -190,16 +210,26 @@ int mla_tree_verify_read_device_error(const void* workspace, uint32_t* flags_out
  *     calls whose kernels overlap on the GPU (other streams, other threads)
  *     race on it, so serialise them;
  *   - the device error word is cleared (an asynchronous 4-byte memset on
- *     `stream`) at the start of each call; it is not reported back by this
- *     entry point;
+ *     `stream`) at the start of each call; read it back with
+ *     mla_tree_verify_read_static_device_error;
  *   - no cudaMalloc, cudaFree or other allocating call is made.
  * Arguments are those of mla_tree_verify_run without the workspace.
  */
 int mla_tree_verify_run_static(const mtv_plan_t* plan, const void* q, const void* kv_pool,
-                               int64_t num_slots, const int64_t* kv_indices, const int32_t* kv_indptr,
-                               const int64_t* out_cache_loc, const int64_t* qo_indptr,
-                               const uint8_t* custom_mask, const int64_t* mask_indptr, float scale,
-                               void* out, float* lse, void* stream);
+                               int64_t num_slots, const int64_t* kv_indices, int64_t kv_indices_len,
+                               const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                               int64_t out_cache_loc_len, const int64_t* qo_indptr,
+                               const uint8_t* custom_mask, int64_t custom_mask_len,
+                               const int64_t* mask_indptr, float scale, void* out, float* lse,
+                               void* stream);
+
+/* Copy the device error word of the fixed scratch used by
+ * mla_tree_verify_run_static on the current device (the bits the kernels of
+ * the static calls since the last one's clear have set; 0 before any static
+ * call) to *flags_out.  Synchronises `stream`; allocates nothing.  Like the
+ * first static call, its first call on a device looks up the scratch address:
+ * make it outside stream capture. */
+int mla_tree_verify_read_static_device_error(uint32_t* flags_out, void* stream);
 
 #ifdef __cplusplus
 }

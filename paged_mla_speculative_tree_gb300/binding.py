@@ -16,13 +16,14 @@ MTV_OK = 0
 MASK_FULL_ROW = 0
 MASK_TREE_ONLY = 1
 FLAG_SIMT_FLOOR = 0x1
+FLAG_TEST_SHORT_WAITS = 0x100  # test only: pipeline waits give up at once (timeout path)
 DEVERR_SLOT_RANGE = 0x1
 DEVERR_INDPTR = 0x2
 DEVERR_TIMEOUT = 0x4
 DEVERR_PARENT = 0x8
 DEVERR_PREFIX = 0x10
 PLAN_MAGIC = 0x4D545650
-ABI_VERSION = 1
+ABI_VERSION = 2
 
 
 class MtvPlan(ctypes.Structure):
@@ -53,7 +54,7 @@ class MtvError(RuntimeError):
 _lib = None
 SYMBOLS = ("mla_tree_verify_plan", "mla_tree_verify_run", "mla_tree_verify_strerror",
            "mla_tree_verify_clear_device_error", "mla_tree_verify_read_device_error",
-           "mla_tree_verify_run_static", "mla_tree_mask_build", "mla_tree_accept", "mla_kv_defrag",
+           "mla_tree_verify_run_static", "mla_tree_verify_read_static_device_error", "mla_tree_mask_build", "mla_tree_accept", "mla_kv_defrag",
            "mla_tree_group_prefix")
 
 
@@ -74,7 +75,7 @@ def load(path: str | None = None):
     lib.mla_tree_verify_plan.argtypes = [I32, I32, I32, I64, I64, I32, I32, I32, I32, I32, I32,
                                          ctypes.POINTER(MtvPlan), ctypes.POINTER(U64)]
     lib.mla_tree_verify_plan.restype = I32
-    lib.mla_tree_verify_run.argtypes = [ctypes.POINTER(MtvPlan), P, P, I64, P, P, P, P, P, P,
+    lib.mla_tree_verify_run.argtypes = [ctypes.POINTER(MtvPlan), P, P, I64, P, I64, P, P, I64, P, P, I64, P,
                                         ctypes.c_float, P, P, P, U64, P]
     lib.mla_tree_verify_run.restype = I32
     lib.mla_tree_verify_strerror.argtypes = [I32]
@@ -83,9 +84,11 @@ def load(path: str | None = None):
     lib.mla_tree_verify_clear_device_error.restype = I32
     lib.mla_tree_verify_read_device_error.argtypes = [P, ctypes.POINTER(ctypes.c_uint32), P]
     lib.mla_tree_verify_read_device_error.restype = I32
-    lib.mla_tree_verify_run_static.argtypes = [ctypes.POINTER(MtvPlan), P, P, I64, P, P, P, P, P, P,
-                                               ctypes.c_float, P, P, P]
+    lib.mla_tree_verify_run_static.argtypes = [ctypes.POINTER(MtvPlan), P, P, I64, P, I64, P, P, I64, P, P,
+                                               I64, P, ctypes.c_float, P, P, P]
     lib.mla_tree_verify_run_static.restype = I32
+    lib.mla_tree_verify_read_static_device_error.argtypes = [ctypes.POINTER(ctypes.c_uint32), P]
+    lib.mla_tree_verify_read_static_device_error.restype = I32
     lib.mla_tree_mask_build.argtypes = [P, P, P, I32, I32, I32, P, U64, P, P, P]
     lib.mla_tree_mask_build.restype = I32
     lib.mla_tree_accept.argtypes = [P, P, P, P, P, P, I32, I32, P, P, P, P, P, P]
@@ -141,17 +144,32 @@ def _stream_handle(stream):
     return int(stream)
 
 
+def _numel(t, given):
+    """Element count of a buffer argument: ``given`` if set, else the tensor's
+    numel (0 for None).  A raw address needs an explicit count."""
+    if given is not None:
+        return int(given)
+    if t is None:
+        return 0
+    if isinstance(t, torch.Tensor):
+        return t.numel()
+    raise ValueError("a raw device address needs an explicit length")
+
+
 def run(p: MtvPlan, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr, custom_mask,
-        mask_indptr, scale: float, out, lse, workspace, stream=None, check: bool = True) -> int:
-    """Enqueues one verify-attention pass; returns the ABI code (raises if check)."""
+        mask_indptr, scale: float, out, lse, workspace, stream=None, check: bool = True,
+        kv_indices_len=None, out_cache_loc_len=None, custom_mask_len=None) -> int:
+    """Enqueues one verify-attention pass; returns the ABI code (raises if check).
+    Buffer lengths default to the tensors' element counts."""
     num_slots = kv_pool.shape[0] if isinstance(kv_pool, torch.Tensor) else 0
     ws_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else 0
     wsp = _ptr(workspace, torch.uint8, "workspace")
     rc = load().mla_tree_verify_run(
         ctypes.byref(p), _ptr(q, torch.bfloat16, "q", wsp), _ptr(kv_pool, torch.bfloat16, "kv_pool", wsp),
-        int(num_slots), _ptr(kv_indices, torch.int64, "kv_indices", wsp),
+        int(num_slots), _ptr(kv_indices, torch.int64, "kv_indices", wsp), _numel(kv_indices, kv_indices_len),
         _ptr(kv_indptr, torch.int32, "kv_indptr"), _ptr(out_cache_loc, torch.int64, "out_cache_loc", wsp),
-        _ptr(qo_indptr, torch.int64, "qo_indptr"), _ptr(custom_mask, torch.uint8, "custom_mask", wsp),
+        _numel(out_cache_loc, out_cache_loc_len), _ptr(qo_indptr, torch.int64, "qo_indptr"),
+        _ptr(custom_mask, torch.uint8, "custom_mask", wsp), _numel(custom_mask, custom_mask_len),
         _ptr(mask_indptr, torch.int64, "mask_indptr"), float(scale),
         _ptr(out, torch.bfloat16, "out", wsp), _ptr(lse, torch.float32, "lse", wsp),
         wsp, int(ws_bytes), _stream_handle(stream))
@@ -161,21 +179,32 @@ def run(p: MtvPlan, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr,
 
 
 def run_static(p: MtvPlan, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr, custom_mask,
-               mask_indptr, scale: float, out, lse, stream=None, check: bool = True) -> int:
+               mask_indptr, scale: float, out, lse, stream=None, check: bool = True,
+               kv_indices_len=None, out_cache_loc_len=None, custom_mask_len=None) -> int:
     """The allocation-free entry point: like ``run`` without a workspace (the
     library's fixed device scratch is used; see the header for its limits)."""
     num_slots = kv_pool.shape[0] if isinstance(kv_pool, torch.Tensor) else 0
     anyp = _ptr(out, torch.bfloat16, "out")
     rc = load().mla_tree_verify_run_static(
         ctypes.byref(p), _ptr(q, torch.bfloat16, "q", anyp), _ptr(kv_pool, torch.bfloat16, "kv_pool", anyp),
-        int(num_slots), _ptr(kv_indices, torch.int64, "kv_indices", anyp),
+        int(num_slots), _ptr(kv_indices, torch.int64, "kv_indices", anyp), _numel(kv_indices, kv_indices_len),
         _ptr(kv_indptr, torch.int32, "kv_indptr"), _ptr(out_cache_loc, torch.int64, "out_cache_loc", anyp),
-        _ptr(qo_indptr, torch.int64, "qo_indptr"), _ptr(custom_mask, torch.uint8, "custom_mask", anyp),
+        _numel(out_cache_loc, out_cache_loc_len), _ptr(qo_indptr, torch.int64, "qo_indptr"),
+        _ptr(custom_mask, torch.uint8, "custom_mask", anyp), _numel(custom_mask, custom_mask_len),
         _ptr(mask_indptr, torch.int64, "mask_indptr"), float(scale), anyp,
         _ptr(lse, torch.float32, "lse"), _stream_handle(stream))
     if check and rc != MTV_OK:
         raise MtvError(rc, "mla_tree_verify_run_static")
     return rc
+
+
+def read_static_device_error(stream=None) -> int:
+    """Error word of the fixed scratch of ``run_static`` on the current device (syncs)."""
+    v = ctypes.c_uint32(0)
+    rc = load().mla_tree_verify_read_static_device_error(ctypes.byref(v), _stream_handle(stream))
+    if rc != MTV_OK:
+        raise MtvError(rc, "mla_tree_verify_read_static_device_error")
+    return int(v.value)
 
 
 def clear_device_error(workspace, stream=None):
@@ -272,14 +301,16 @@ class MlaTreeVerify:
         clear_device_error(self.workspace)
 
     def __call__(self, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr, custom_mask,
-                 mask_indptr, scale, out=None, lse=None, stream=None):
+                 mask_indptr, scale, out=None, lse=None, stream=None, **lengths):
+        """``lengths``: optional kv_indices_len / out_cache_loc_len /
+        custom_mask_len (default: the tensors' element counts)."""
         T = self.plan.total_q_max
         if out is None:
             out = torch.empty((T, 64, 512), dtype=torch.bfloat16, device=self.device)
         if lse is None:
             lse = torch.empty((T, 64), dtype=torch.float32, device=self.device)
         run(self.plan, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr, custom_mask,
-            mask_indptr, scale, out, lse, self.workspace, stream)
+            mask_indptr, scale, out, lse, self.workspace, stream, **lengths)
         return out, lse
 
     def device_error(self, stream=None) -> int:

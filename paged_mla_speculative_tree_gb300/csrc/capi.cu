@@ -64,7 +64,7 @@ int mla_tree_verify_plan(int device, int bs, int max_q_per_req, int64_t total_q_
   if (bs < 0 || max_q_per_req < 0 || total_q_max < 0 || max_prefix < 0 || nsplit_override < 0)
     return MTV_E_BAD_ARGUMENT;
   if (mask_layout != MTV_MASK_FULL_ROW && mask_layout != MTV_MASK_TREE_ONLY) return MTV_E_BAD_ARGUMENT;
-  if (flags & ~MTV_FLAG_SIMT_FLOOR) return MTV_E_BAD_ARGUMENT;
+  if (flags & ~(MTV_FLAG_SIMT_FLOOR | MTV_FLAG_TEST_SHORT_WAITS)) return MTV_E_BAD_ARGUMENT;
   int ndev = 0;
   if (cudaGetDeviceCount(&ndev) != cudaSuccess || device < 0 || device >= ndev) {
     cudaGetLastError();
@@ -142,18 +142,22 @@ int mla_tree_verify_plan(int device, int bs, int max_q_per_req, int64_t total_q_
 }
 
 int mla_tree_verify_run(const mtv_plan_t* plan, const void* q, const void* kv_pool,
-                        int64_t num_slots, const int64_t* kv_indices, const int32_t* kv_indptr,
-                        const int64_t* out_cache_loc, const int64_t* qo_indptr,
-                        const uint8_t* custom_mask, const int64_t* mask_indptr, float scale,
-                        void* out, float* lse, void* workspace, uint64_t workspace_bytes,
-                        void* stream) {
+                        int64_t num_slots, const int64_t* kv_indices, int64_t kv_indices_len,
+                        const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                        int64_t out_cache_loc_len, const int64_t* qo_indptr,
+                        const uint8_t* custom_mask, int64_t custom_mask_len,
+                        const int64_t* mask_indptr, float scale, void* out, float* lse,
+                        void* workspace, uint64_t workspace_bytes, void* stream) {
   if (!plan) return MTV_E_NULL_POINTER;
   if (plan->magic != MTV_PLAN_MAGIC || plan->version != MTV_ABI_VERSION) return MTV_E_BAD_PLAN;
   if (!workspace || !kv_indptr || !qo_indptr || !mask_indptr) return MTV_E_NULL_POINTER;
-  if (plan->bs > 0 && plan->total_q_max > 0 &&
-      (!q || !kv_pool || !kv_indices || !out_cache_loc || !custom_mask || !out || !lse))
+  if (kv_indices_len < 0 || out_cache_loc_len < 0 || custom_mask_len < 0) return MTV_E_BAD_ARGUMENT;
+  if ((kv_indices_len > 0 && !kv_indices) || (out_cache_loc_len > 0 && !out_cache_loc) ||
+      (custom_mask_len > 0 && !custom_mask))
     return MTV_E_NULL_POINTER;
-  if (num_slots < 0 || num_slots > INT32_MAX) return MTV_E_BAD_ARGUMENT;  // TMA row coordinates are 32-bit
+  if (plan->bs > 0 && plan->total_q_max > 0 && (!q || !kv_pool || !out || !lse)) return MTV_E_NULL_POINTER;
+  // The gather warps hold a checked slot in a 32-bit register.
+  if (num_slots < 0 || num_slots > INT32_MAX) return MTV_E_BAD_ARGUMENT;
   if (reinterpret_cast<uintptr_t>(kv_pool) & 15) return MTV_E_BAD_ARGUMENT;
   if (reinterpret_cast<uintptr_t>(workspace) & 255) return MTV_E_WORKSPACE_ALIGN;
   if (workspace_bytes < plan->ws_bytes) return MTV_E_WORKSPACE_SMALL;
@@ -176,6 +180,9 @@ int mla_tree_verify_run(const mtv_plan_t* plan, const void* q, const void* kv_po
   P.qo_indptr = qo_indptr;
   P.custom_mask = custom_mask;
   P.mask_indptr = mask_indptr;
+  P.kv_indices_len = kv_indices_len;
+  P.out_cache_loc_len = out_cache_loc_len;
+  P.custom_mask_len = custom_mask_len;
   P.scale = scale;
   P.scale_log2 = scale * kLog2e;
   P.out = static_cast<__nv_bfloat16*>(out);
@@ -193,6 +200,8 @@ int mla_tree_verify_run(const mtv_plan_t* plan, const void* q, const void* kv_po
   P.total_q_max = plan->total_q_max;
   P.max_prefix = plan->max_prefix;
   P.split_keys = plan->split_keys;
+  // ~1 s at the GB300's clock; the test flag makes any wait that has to spin give up
+  P.wait_cycles = (plan->flags & MTV_FLAG_TEST_SHORT_WAITS) ? 0ll : (1ll << 31);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = (plan->flags & MTV_FLAG_SIMT_FLOOR) ? launch_partial_simt(P, st)

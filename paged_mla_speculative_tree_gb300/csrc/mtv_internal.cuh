@@ -28,6 +28,7 @@ struct Params {
   const int64_t* qo_indptr;
   const uint8_t* custom_mask;
   const int64_t* mask_indptr;
+  int64_t kv_indices_len, out_cache_loc_len, custom_mask_len;  // elements readable at each buffer
   float scale;       // natural-log domain score scale
   float scale_log2;  // scale * log2(e)
   __nv_bfloat16* out;  // [total_q, 64, 512]
@@ -37,10 +38,14 @@ struct Params {
   unsigned* err;       // sticky device error word
   int bs, max_q, mask_layout, nsplit, grid_rows, key_tile;
   int64_t total_q_max, max_prefix, split_keys;
+  long long wait_cycles;  // bound of one pipeline wait before the kernel gives up
 };
 
-// Per-request geometry read from the device CSR buffers, validated against
-// the plan bounds.  ok == false: the request is skipped (error bit set).
+// Per-request geometry read from the device CSR buffers and validated before
+// any of it is used as an offset: the plan bounds, monotone offsets, and every
+// range the request will index (kv_indices, out_cache_loc and q rows, its mask
+// block) inside the buffer lengths given to the run.  ok == false: the request
+// is skipped (error bit set, p = n = 0, nothing of it is read or written).
 struct Req {
   int64_t p, n, kv_off, q_off, mask_off, keys;
   bool ok;
@@ -56,8 +61,16 @@ __device__ __forceinline__ Req load_req(const Params& P, int r) {
   R.p = k1 - k0;
   R.n = q1 - q0;
   R.keys = R.p + R.n;
-  R.ok = (R.p >= 0 && R.n >= 0 && R.p <= P.max_prefix && R.n <= P.max_q && q0 >= 0 &&
-          q1 <= P.total_q_max && k0 >= 0 && R.mask_off >= 0);
+  bool ok = R.p >= 0 && R.n >= 0 && R.p <= P.max_prefix && R.n <= P.max_q && q0 >= 0 &&
+            q1 <= P.total_q_max && q1 <= P.out_cache_loc_len && k0 >= 0 && k1 <= P.kv_indices_len &&
+            R.mask_off >= 0 && R.mask_off <= P.custom_mask_len;
+  if (ok && R.n > 0) {
+    // mask block of n rows x (p + n) (FULL_ROW) or n (TREE_ONLY) bytes; the
+    // division keeps the product from overflowing
+    const int64_t row = (P.mask_layout == MTV_MASK_FULL_ROW) ? R.keys : R.n;
+    ok = row <= (P.custom_mask_len - R.mask_off) / R.n;
+  }
+  R.ok = ok;
   if (!R.ok) {
     atomicOr(P.err, MTV_DEVERR_INDPTR);
     R.p = R.n = R.keys = 0;

@@ -41,9 +41,17 @@
 // CTA 0 (or the final bf16 output when there is one split).
 //
 // TMEM (512 columns): O half [0,256), partial S [256,320), latent Q half
-// [320,448), P double buffer [448,512).  Every wait is bounded: a timeout sets
-// MTV_DEVERR_TIMEOUT and the CTA winds down (its MMAs and copies drain, TMEM
-// is freed) instead of hanging.
+// [320,448), P double buffer [448,512).
+//
+// Every pipeline wait is bounded (Params::wait_cycles).  A wait that gives up
+// sets MTV_DEVERR_TIMEOUT and the abort flag of both CTAs of the pair, and
+// every role leaves its loop.  The wind-down then runs with its own bound and
+// ignores the abort flag: the MMA issuer waits for a final commit (every MMA
+// it issued has completed), the gather warps wait for their copies, each
+// softmax warp tells the peer how many score tiles it sent, and after a
+// cluster barrier each CTA waits for exactly those incoming bulk copies.
+// Only then is TMEM freed and, after a second cluster barrier, the CTA exits:
+// no tensor-core operation, copy or remote write is in flight past that point.
 //
 // Building with -DMTV_TRACE records clock64() timestamps of the pipeline
 // events of the first CTA into a device buffer (read with mtv_trace_read).
@@ -84,7 +92,7 @@ constexpr int NTHREADS = 32 * (1 + NPROD_WARPS + NSOFT_WARPS);  // warp 0 MMA, t
 constexpr int KSTEPS2 = NK / 16;          // 4
 constexpr float kRescaleLog2 = 8.0f;      // move the reference max only past 2^8 growth
 constexpr float kQuantMagic = 12615680.0f;  // 1.5 * 2^23 + 2^15
-constexpr long long kTimeoutCycles = 1ll << 31;
+constexpr long long kDrainCycles = 1ll << 31;  // bound of each wind-down wait (~1 s)
 constexpr int kMaxKeysPerGatherWarp = (NK + NPROD_WARPS - 1) / NPROD_WARPS;
 constexpr int kRopeGroups = (kMaxKeysPerGatherWarp + 7) / 8;  // rope copies: 8 keys x 4 lanes per instruction
 
@@ -111,7 +119,8 @@ constexpr uint32_t kOffLsum = kOffRowMax + kRowMaxBytes;          // [WPQ][128 r
 constexpr uint32_t kLsumBytes = WPQ * ROWS * 4;
 constexpr uint32_t kOffBars = kOffLsum + kLsumBytes;
 constexpr uint32_t kOffCtl = kOffBars + 256;
-constexpr uint32_t kSmemBytes = kOffCtl + 64 + 1024;  // + slack for 1 KB alignment
+constexpr uint32_t kCtlBytes = 256;
+constexpr uint32_t kSmemBytes = kOffCtl + kCtlBytes + 1024;  // + slack for 1 KB alignment
 
 constexpr uint32_t kTmemO = 0, kTmemS = 256, kTmemQ = 320, kTmemP = 448;
 
@@ -129,8 +138,12 @@ static_assert(kXRegion % 16 == 0 && kOffRx % 16 == 0 && kOffTx % 16 == 0, "bulk 
 
 struct Ctl {
   uint32_t tmem_base;
-  volatile int abort;
+  volatile int abort;           // set by a wait of this CTA or of the peer that gave up
+  int armed;                    // score-exchange phases armed with the expected bytes
+  int waited[NSOFT_WARPS];      // per softmax warp: exchange phases it saw complete
+  int peer_sent[NSOFT_WARPS];   // written by the peer: score tiles each of its warps sent here
 };
+static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 
 #ifdef MTV_TRACE
 constexpr int kTraceTiles = 128, kTraceEvents = 16;
@@ -151,24 +164,53 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// Bounded wait on a CTA barrier; false (and abort) on timeout or abort.
-__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl, unsigned* err, bool cluster) {
-  if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+// What a wait needs to give up: the flags of this CTA, the error word, the
+// bound, and the cluster address of the peer's abort flag.
+struct Waiter {
+  Ctl* ctl;
+  unsigned* err;
+  long long limit;
+  uint32_t peer_abort;
+};
+
+// Timeout: record it and stop both CTAs of the pair.
+__device__ __noinline__ void give_up(Ctl* ctl, unsigned* err, uint32_t peer_abort) {
+  ctl->abort = 1;
+  st_cluster_u32(peer_abort, 1u);
+  atomicOr(err, MTV_DEVERR_TIMEOUT);
+}
+
+// Bounded wait on a CTA barrier; false on timeout (after give_up) or abort.
+__device__ __noinline__ bool wait_bar(uint32_t bar, uint32_t parity, Ctl* ctl, unsigned* err, long long limit,
+                                      uint32_t peer_abort) {
+  if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   for (;;) {
-    if (cluster ? mbar_try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait(bar, parity)) return true;
     if (ctl->abort) return false;
-    if (clock64() - t0 > kTimeoutCycles) {
-      ctl->abort = 1;
-      atomicOr(err, MTV_DEVERR_TIMEOUT);
+    if (clock64() - t0 > limit) {
+      give_up(ctl, err, peer_abort);
       return false;
     }
   }
 }
 
 // Inline fast path: most waits find the phase already complete.
-__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, Ctl* ctl, unsigned* err) {
-  return mbar_try_wait(bar, parity) || wait_bar(bar, parity, ctl, err, false);
+__device__ __forceinline__ bool wait_fast(uint32_t bar, uint32_t parity, const Waiter& w) {
+  return mbar_try_wait(bar, parity) || wait_bar(bar, parity, w.ctl, w.err, w.limit, w.peer_abort);
+}
+
+// Wind-down wait: ignores the abort flag; its own bound only guards against a
+// broken device (it sets the timeout bit and returns false).
+__device__ __noinline__ bool drain_wait(uint32_t bar, uint32_t parity, unsigned* err) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kDrainCycles) {
+      atomicOr(err, MTV_DEVERR_TIMEOUT);
+      return false;
+    }
+  }
+  return true;
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial_tc_kernel(const Params P) {
@@ -230,6 +272,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     mbar_init(bar(B_FIN), 1);
     for (int qq = 0; qq < 4; ++qq) mbar_init(bar(B_QMAX + qq), WPQ);
     ctl->abort = 0;
+    ctl->armed = 0;
+    for (int w = 0; w < NSOFT_WARPS; ++w) ctl->waited[w] = ctl->peer_sent[w] = 0;
     fence_mbar_init_cluster();
   }
   if (warp == 0) {
@@ -239,9 +283,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  cluster_sync();  // barriers of both CTAs initialised before any remote access
+  cluster_sync();  // barriers and control blocks of both CTAs initialised before any remote access
   if (threadIdx.x == 0) MTV_TR(1, kTraceTiles - 1, 1);
   const uint32_t tmem = ctl->tmem_base;
+  const Waiter W{ctl, P.err, P.wait_cycles, mapa(smem_u32(const_cast<int*>(&ctl->abort)), peer)};
 
   if (warp == 0) {
     // ------------------------------------------------------------ MMA issuer
@@ -287,7 +332,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       // not hold back the GEMM2 that frees an earlier one.  Tensor-core
       // operations of one thread run in issue order, and GEMM2(j) is only
       // issued after GEMM1(j).
-      bool ok = wait_bar(bar(B_Q_READY), 0, ctl, P.err, false);
+      bool ok = wait_fast(bar(B_Q_READY), 0, W);
       int j1 = 0, j2 = 0;
       long long t_prog = clock64();
       while (ok && j2 < T) {
@@ -308,16 +353,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
           t_prog = clock64();
         } else {
           if (ctl->abort) break;
-          if (clock64() - t_prog > kTimeoutCycles) {
-            ctl->abort = 1;
-            atomicOr(P.err, MTV_DEVERR_TIMEOUT);
+          if (clock64() - t_prog > W.limit) {
+            give_up(ctl, P.err, W.peer_abort);
             break;
           }
           __nanosleep(32);
         }
       }
-      mma_commit(bar(B_FIN));  // drains every MMA issued above
-      wait_bar(bar(B_FIN), 0, ctl, P.err, false);
+      // Every MMA issued above has completed once B_FIN arrives (tensor-core
+      // operations of one thread complete in order); waited for even after an
+      // abort, since TMEM is freed below.
+      mma_commit(bar(B_FIN));
+      drain_wait(bar(B_FIN), 0, P.err);
     }
     __syncwarp();
   } else if (warp <= NPROD_WARPS) {
@@ -364,7 +411,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       const uint32_t vlo = __reduce_or_sync(0xffffffffu, (slot >= 0 && kk_l < 32) ? 1u << kk_l : 0u);
       const uint32_t vhi = __reduce_or_sync(0xffffffffu, (slot >= 0 && kk_l >= 32) ? 1u << (kk_l - 32) : 0u);
       if (j >= STAGES) {
-        bool ok = wait_bar(bar(B_KV_EMPTY + s), ((j / STAGES) - 1) & 1, ctl, P.err, false);
+        bool ok = wait_fast(bar(B_KV_EMPTY + s), ((j / STAGES) - 1) & 1, W);
         if (!__all_sync(0xffffffffu, ok)) break;
       }
       if (pw == 0 && lane == 0) MTV_TR(1, j, 0);
@@ -471,6 +518,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     float m_ref = -INFINITY, l = 0.f;
     bool alive = true;
     uint32_t s[NCOL];  // this CTA's partial scores of the tile being finished
+    // wind-down bookkeeping: tiles this warp sent to the peer, exchange phases
+    // it saw complete, and (tracer) phases armed with their expected bytes
+    int nsent = 0, nwaited = 0, narmed = 0;
 
     // Load tile jn's partial scores from TMEM and send them to the peer as
     // NCOL 16-bit integers with a shared exponent k (max|v| < 2^k):
@@ -479,7 +529,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     // spacing is 1, and its low 16 mantissa bits are rint(y) + 2^15.  The
     // receiver rebuilds 1.5*2^23 + u as float bits and subtracts exactly.
     auto fetch_and_send = [&](int jn) -> bool {
-      bool ok = wait_fast(bar(B_S_FULL), jn & 1, ctl, P.err);
+      bool ok = wait_fast(bar(B_S_FULL), jn & 1, W);
       if (!__all_sync(0xffffffffu, ok)) return false;
       if (tracer) MTV_TR(2, jn, 0);
       tc_fence_after();
@@ -518,18 +568,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       if (lane == 0)
         bulk_copy_to_peer(rx_peer + uint32_t(jn & 1) * kXBytes, tx + uint32_t(wreg) * kXRegion, kXRegion,
                           peer_sx_full + 8u * uint32_t(jn & 1));
+      ++nsent;
       if (tracer) MTV_TR(2, jn, 1);
       if (tracer2) MTV_TR(3, jn, 1);
       return true;
     };
 
     if (tracer) mbar_arrive_expect_tx(bar(B_SX_FULL0), kXBytes);  // tile 0
+    narmed = 1;
     alive = fetch_and_send(0);
     for (int j = 0; alive && j < T; ++j) {
       // tile j+1's bytes land in buffer (j+1)&1, whose previous phase (tile j-1) is complete
-      if (tracer && j + 1 < T) mbar_arrive_expect_tx(bar(B_SX_FULL0 + ((j + 1) & 1)), kXBytes);
-      bool ok = wait_fast(bar(B_SX_FULL0 + (j & 1)), (j >> 1) & 1, ctl, P.err);
+      if (j + 1 < T) {
+        if (tracer) mbar_arrive_expect_tx(bar(B_SX_FULL0 + ((j + 1) & 1)), kXBytes);
+        narmed = j + 2;
+      }
+      bool ok = wait_fast(bar(B_SX_FULL0 + (j & 1)), (j >> 1) & 1, W);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+      nwaited = j + 1;
       if (tracer) MTV_TR(2, j, 2);
       if (tracer2) MTV_TR(3, j, 2);
       float x[NCOL];  // full scores of this warp's columns: own exact partial + peer's
@@ -563,7 +619,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
 
       // tree mask (raw units; masked -> -inf)
       const int sidx = j % STAGES;
-      ok = wait_fast(bar(B_KV_FULL + sidx), (j / STAGES) & 1, ctl, P.err);
+      ok = wait_fast(bar(B_KV_FULL + sidx), (j / STAGES) & 1, W);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
       if (tracer) MTV_TR(2, j, 8);
       uint64_t vm = 0;  // OR of the gather warps' masks (exactly NPROD_WARPS words are written)
@@ -597,7 +653,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       // combine the tile max of the WPQ warps of this row (bounded mbarrier meeting)
       __syncwarp();
       if (lane == 0) mbar_arrive(qbar);
-      ok = wait_fast(qbar, j & 1, ctl, P.err);
+      ok = wait_fast(qbar, j & 1, W);
       if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
 #pragma unroll
       for (int hh = 0; hh < WPQ; ++hh) mt = fmaxf(mt, rowmax[((j & 1) * WPQ + hh) * ROWS + rr]);
@@ -636,11 +692,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       // P buffer j&1 was last read by GEMM2(j-2); O may only be rescaled once
       // GEMM2(j-1) has finished accumulating into it.
       if (j >= 2) {
-        ok = wait_fast(bar(B_O_READY0 + (j & 1)), ((j - 2) >> 1) & 1, ctl, P.err);
+        ok = wait_fast(bar(B_O_READY0 + (j & 1)), ((j - 2) >> 1) & 1, W);
         if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
       }
       if (j >= 1 && __any_sync(0xffffffffu, move)) {  // warp-uniform TMEM read-modify-write of this warp's O columns
-        ok = wait_fast(bar(B_O_READY0 + ((j - 1) & 1)), ((j - 1) >> 1) & 1, ctl, P.err);
+        ok = wait_fast(bar(B_O_READY0 + ((j - 1) & 1)), ((j - 1) >> 1) & 1, W);
         if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
         tc_fence_after();
 #pragma unroll 1
@@ -665,7 +721,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     if (tracer) MTV_TR(2, kTraceTiles - 1, 0);
     // epilogue: normalised O columns of this warp (+ LSE from CTA 0, warp h = 0)
     if (alive) {
-      bool ok = wait_fast(bar(B_O_READY0 + ((T - 1) & 1)), ((T - 1) >> 1) & 1, ctl, P.err);
+      bool ok = wait_fast(bar(B_O_READY0 + ((T - 1) & 1)), ((T - 1) >> 1) & 1, W);
       alive = __all_sync(0xffffffffu, ok);
     }
     // the row's WPQ partial sums meet in shared memory
@@ -673,7 +729,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       lsum_s[h * ROWS + rr] = l;
       __syncwarp();
       if (lane == 0) mbar_arrive(qbar);
-      bool ok = wait_fast(qbar, T & 1, ctl, P.err);
+      bool ok = wait_fast(qbar, T & 1, W);
       alive = __all_sync(0xffffffffu, ok);
     }
     if (alive) {
@@ -734,14 +790,51 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         else P.part_lse[int64_t(split) * P.total_q_max * kHeads + out_row] = lse;
       }
     }
+    // Wind-down bookkeeping (also after an abort): the peer learns how many
+    // score tiles this warp sent it; the tracer records the armed phases.
+    if (lane == 0) {
+      ctl->waited[wreg] = nwaited;
+      st_cluster_u32(mapa(smem_u32(&ctl->peer_sent[wreg]), peer), uint32_t(nsent));
+    }
+    if (tracer) ctl->armed = narmed;
   }
 
+  // ---------------------------------------------------------------- wind-down
+  // Every role has left its loop: the MMA issuer saw its last MMA complete,
+  // the gather warps their copies.  The first cluster barrier publishes the
+  // peer's sent counts and guarantees that every bulk copy into this CTA has
+  // been issued.  Thread 0 then waits for exactly those bytes: phases from the
+  // first one no warp saw complete, each armed (or its arming corrected) with
+  // the bytes of the peer warps that sent that tile.  A warp sends tile j+1
+  // only after seeing tile j arrive, so at most two tiles are outstanding and
+  // they use different buffers.
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  cluster_sync();
+  if (threadIdx.x == 0) {
+    int j = 0;
+    for (int w = 0; w < NSOFT_WARPS; ++w) j = max(j, ctl->waited[w]);
+    for (;; ++j) {
+      int senders = 0;
+      for (int w = 0; w < NSOFT_WARPS; ++w) senders += ctl->peer_sent[w] > j ? 1 : 0;
+      if (senders == 0) break;
+      const uint32_t b = bar(B_SX_FULL0 + (j & 1));
+      const uint32_t bytes = uint32_t(senders) * kXRegion;
+      if (j < ctl->armed) {
+        if (bytes < kXBytes) mbar_complete_tx(b, kXBytes - bytes);  // copies that will never come
+      } else {
+        mbar_arrive_expect_tx(b, bytes);
+      }
+      if (!drain_wait(b, (j >> 1) & 1, P.err)) break;
+    }
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   if (threadIdx.x == 0) MTV_TR(2, kTraceTiles - 1, 2);
   if (warp == 0) tmem_dealloc(tmem, 512);
-  cluster_sync();  // the peer may still arrive on / store into this CTA's shared memory until here
+  cluster_sync();  // both CTAs have received everything sent to them
   if (threadIdx.x == 0) MTV_TR(2, kTraceTiles - 1, 3);
 }
 

@@ -45,10 +45,12 @@ int scratch_address(int device, void** out) {
 }  // namespace
 
 extern "C" int mla_tree_verify_run_static(const mtv_plan_t* plan, const void* q, const void* kv_pool,
-                                          int64_t num_slots, const int64_t* kv_indices, const int32_t* kv_indptr,
-                                          const int64_t* out_cache_loc, const int64_t* qo_indptr,
-                                          const uint8_t* custom_mask, const int64_t* mask_indptr, float scale,
-                                          void* out, float* lse, void* stream) {
+                                          int64_t num_slots, const int64_t* kv_indices, int64_t kv_indices_len,
+                                          const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                                          int64_t out_cache_loc_len, const int64_t* qo_indptr,
+                                          const uint8_t* custom_mask, int64_t custom_mask_len,
+                                          const int64_t* mask_indptr, float scale, void* out, float* lse,
+                                          void* stream) {
   if (!plan) return MTV_E_NULL_POINTER;
   if (plan->magic != MTV_PLAN_MAGIC || plan->version != MTV_ABI_VERSION) return MTV_E_BAD_PLAN;
   if (plan->ws_bytes > kStaticScratchBytes) return MTV_E_WORKSPACE_SMALL;
@@ -67,6 +69,22 @@ extern "C" int mla_tree_verify_run_static(const mtv_plan_t* plan, const void* q,
     cudaGetLastError();
     return MTV_E_CUDA;
   }
-  return mla_tree_verify_run(plan, q, kv_pool, num_slots, kv_indices, kv_indptr, out_cache_loc, qo_indptr,
-                             custom_mask, mask_indptr, scale, out, lse, ws, kStaticScratchBytes, stream);
+  return mla_tree_verify_run(plan, q, kv_pool, num_slots, kv_indices, kv_indices_len, kv_indptr, out_cache_loc,
+                             out_cache_loc_len, qo_indptr, custom_mask, custom_mask_len, mask_indptr, scale, out,
+                             lse, ws, kStaticScratchBytes, stream);
+}
+
+// The error word sits at the head of the same fixed array, so reading it
+// back needs only the array's device address (no allocation either).
+extern "C" int mla_tree_verify_read_static_device_error(uint32_t* flags_out, void* stream) {
+  if (!flags_out) return MTV_E_NULL_POINTER;
+  int device = -1;
+  if (cudaGetDevice(&device) != cudaSuccess) {
+    cudaGetLastError();
+    return MTV_E_CUDA;
+  }
+  void* ws = nullptr;
+  const int rc = scratch_address(device, &ws);
+  if (rc != MTV_OK) return rc;
+  return mla_tree_verify_read_device_error(ws, flags_out, stream);
 }

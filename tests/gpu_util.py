@@ -20,7 +20,7 @@ def to_device(wl, dev="cuda"):
 
 
 def run_gpu(wl, flags=0, nsplit=0, dev_tensors=None, total_q_max=None, max_prefix=None, max_q=None,
-            return_err=False):
+            return_err=False, lengths=None):
     d = dev_tensors or to_device(wl)
     T = total_q_max or wl.total_q
     m = binding.MlaTreeVerify(wl.bs, max_q or wl.max_q_per_req, T, max_prefix or wl.max_prefix,
@@ -29,7 +29,7 @@ def run_gpu(wl, flags=0, nsplit=0, dev_tensors=None, total_q_max=None, max_prefi
     out = torch.full((T, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((T, 64), float("nan"), dtype=torch.float32, device="cuda")
     m(d["q"], d["kv_pool"], d["kv_indices"], d["kv_indptr"], d["out_cache_loc"], d["qo_indptr"],
-      d["custom_mask"], d["mask_indptr"], wl.scale, out, lse)
+      d["custom_mask"], d["mask_indptr"], wl.scale, out, lse, **(lengths or {}))
     torch.cuda.synchronize()
     err = m.device_error()
     o = out.float().cpu().reshape(-1, 512).numpy()

@@ -84,13 +84,16 @@ def test_plan_rejects_bad_arguments_before_touching_a_device(lib):
     assert _plan_rc(lib, layout=7) == -3
     assert _plan_rc(lib, bs=-1) == -3
     assert _plan_rc(lib, flags=0x10) == -3
+    assert _plan_rc(lib, flags=0x200) == -3
     assert lib.mla_tree_verify_plan(0, 1, 8, 8, 256, 64, 512, 64, 0, 0, 0, None, None) == -1
 
 
 def test_run_host_checks(lib):
     P = binding.MtvPlan()
     fake = ctypes.c_void_p(0x100000)  # never dereferenced: checks fail first
-    args = [fake, fake, 4096, fake, fake, fake, fake, fake, fake, 1.0, fake, fake]
+    # q, kv_pool, num_slots, kv_indices, len, kv_indptr, out_cache_loc, len, qo_indptr, custom_mask, len,
+    # mask_indptr, scale, out, lse
+    args = [fake, fake, 4096, fake, 64, fake, fake, 8, fake, fake, 64, fake, 1.0, fake, fake]
     # not a plan
     assert lib.mla_tree_verify_run(ctypes.byref(P), *args, fake, 1 << 20, None) == -6
     assert lib.mla_tree_verify_run(None, *args, fake, 1 << 20, None) == -1
@@ -102,9 +105,25 @@ def test_run_host_checks(lib):
     nulls = list(args)
     nulls[0] = None  # q
     assert lib.mla_tree_verify_run(ctypes.byref(P), *nulls, fake, 1 << 20, None) == -1
+    # buffer lengths: negative -> bad argument; NULL with a positive length -> null pointer;
+    # NULL with length 0 is allowed (nothing may be read there)
+    for i in (4, 7, 10):
+        bad = list(args)
+        bad[i] = -1
+        assert lib.mla_tree_verify_run(ctypes.byref(P), *bad, fake, 1 << 20, None) == -3
+        bad = list(args)
+        bad[i - 1] = None
+        assert lib.mla_tree_verify_run(ctypes.byref(P), *bad, fake, 1 << 20, None) == -1
+    big = list(args)
+    big[2] = 1 << 31  # num_slots past the 32-bit slot register of the gather
+    assert lib.mla_tree_verify_run(ctypes.byref(P), *big, fake, 1 << 20, None) == -3
     assert lib.mla_tree_verify_clear_device_error(None, None) == -1
     v = ctypes.c_uint32()
     assert lib.mla_tree_verify_read_device_error(None, ctypes.byref(v), None) == -1
+    assert lib.mla_tree_verify_read_static_device_error(None, None) == -1
+    # the static entry rejects a foreign plan before touching a device
+    P.magic = 0
+    assert lib.mla_tree_verify_run_static(ctypes.byref(P), *args, None) == -6
 
 
 def test_tree_ops_host_checks(lib):

@@ -109,6 +109,86 @@ def test_bad_slot_sets_error_and_is_masked(flags):
     G.compare(wl, out, lse, ref=ref, tag="bad slot")
 
 
+def _padded(t, extra):
+    """Device copy of t followed by `extra` zero elements: a declared length
+    shorter than the allocation lets a test present offsets past the declared
+    end while every byte a kernel could touch is still allocated."""
+    buf = torch.zeros(t.numel() + extra, dtype=t.dtype, device="cuda")
+    buf[:t.numel()].copy_(t)
+    return buf
+
+
+def _rows_of(wl, reqs):
+    H = wl.num_heads
+    qop = wl.qo_indptr.numpy()
+    return np.concatenate([np.arange(qop[r] * H, qop[r + 1] * H) for r in reqs]).astype(np.int64)
+
+
+def _three_offset_cases():
+    g = torch.Generator().manual_seed(91)
+    parents = [W.random_parents(n, g) for n in (5, 7, 3, 6)]
+    return W.custom([100, 130, 90, 70], parents, 2048, seed=92)
+
+
+def test_mask_block_past_custom_mask_end_is_flagged_and_skipped(flags):
+    # request 1's mask block starts 3 bytes before the declared end of custom_mask
+    wl = _three_offset_cases()
+    d = G.to_device(wl)
+    d["custom_mask"] = _padded(wl.custom_mask, 1 << 16)
+    mip = wl.mask_indptr.clone()
+    mip[1] = wl.custom_mask.numel() - 3
+    d["mask_indptr"] = mip.cuda()
+    out, lse, err, _ = G.run_gpu(wl, flags, nsplit=2, dev_tensors=d, return_err=True,
+                                 lengths={"custom_mask_len": wl.custom_mask.numel()})
+    assert err & binding.DEVERR_INDPTR
+    bad = _rows_of(wl, [1])
+    assert np.all(np.isnan(out[bad])) and np.all(np.isnan(lse[bad]))  # skipped: rows untouched
+    G.compare(wl, out, lse, rows=_rows_of(wl, [0, 2, 3]), tag="mask past end")
+
+
+def test_kv_indptr_past_kv_indices_end_is_flagged_and_skipped(flags):
+    # kv_indptr[bs] is one past the declared length of kv_indices: the last request is skipped
+    wl = _three_offset_cases()
+    d = G.to_device(wl)
+    d["kv_indices"] = _padded(wl.kv_indices, 4096)
+    out, lse, err, _ = G.run_gpu(wl, flags, nsplit=2, dev_tensors=d, return_err=True,
+                                 lengths={"kv_indices_len": wl.kv_indices.numel() - 1})
+    assert err & binding.DEVERR_INDPTR
+    bad = _rows_of(wl, [3])
+    assert np.all(np.isnan(out[bad])) and np.all(np.isnan(lse[bad]))
+    G.compare(wl, out, lse, rows=_rows_of(wl, [0, 1, 2]), tag="kv_indptr past end")
+
+
+def test_qo_indptr_past_out_cache_loc_end_is_flagged_and_skipped(flags):
+    wl = _three_offset_cases()
+    d = G.to_device(wl)
+    d["out_cache_loc"] = _padded(wl.out_cache_loc, 256)
+    out, lse, err, _ = G.run_gpu(wl, flags, dev_tensors=d, return_err=True,
+                                 lengths={"out_cache_loc_len": wl.out_cache_loc.numel() - 2})
+    assert err & binding.DEVERR_INDPTR
+    bad = _rows_of(wl, [3])
+    assert np.all(np.isnan(out[bad])) and np.all(np.isnan(lse[bad]))
+    G.compare(wl, out, lse, rows=_rows_of(wl, [0, 1, 2]), tag="qo_indptr past end")
+
+
+@pytest.mark.parametrize("nsplit", [1, 3])
+def test_timeout_path_returns_reports_and_leaves_the_context_usable(nsplit):
+    """With the test flag every pipeline wait that has to spin gives up: the
+    tensor-core kernel must wind down (MMAs, gathers and score copies drained,
+    TMEM freed), report MTV_DEVERR_TIMEOUT and return; a normal call in the
+    same process then matches the oracle."""
+    g = torch.Generator().manual_seed(77)
+    parents = [W.random_parents(n, g) for n in (1, 5, 13, 3)]
+    wl = W.custom([0, 77, 300, 129], parents, 2048, seed=78)
+    d = G.to_device(wl)
+    for _ in range(2):
+        _, _, err, _ = G.run_gpu(wl, binding.FLAG_TEST_SHORT_WAITS, nsplit=nsplit, dev_tensors=d,
+                                 return_err=True)
+        assert err & binding.DEVERR_TIMEOUT
+    out, lse = G.run_gpu(wl, 0, nsplit=nsplit, dev_tensors=d)
+    G.compare(wl, out, lse, tag="after timeout")
+
+
 def test_request_beyond_plan_bounds_is_flagged(flags):
     wl = W.custom([300], [W.chain_parents(4)], 1024, seed=15)
     out, lse, err, _ = G.run_gpu(wl, flags, max_prefix=200, return_err=True)

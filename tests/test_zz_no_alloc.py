@@ -46,6 +46,32 @@ def test_static_scratch_entry_matches_workspace_entry_twice():
         # and both agree with the oracle on a sample
         rows = G.sample_rows(wl, 64, seed=3)
         G.compare(wl, o, l, rows=rows, tag="static scratch")
+        assert binding.read_static_device_error() == 0
+
+
+def test_static_scratch_reports_its_error_word_and_allocates_nothing():
+    wl = _wl(53)
+    d = G.to_device(wl)
+    m = binding.MlaTreeVerify(2, 16, wl.total_q, 3000, nsplit=3)
+    out = torch.zeros((wl.total_q, 64, 512), dtype=torch.bfloat16, device="cuda")
+    lse = torch.zeros((wl.total_q, 64), dtype=torch.float32, device="cuda")
+    bad = d["kv_indices"].clone()
+    bad[10] = 1 << 40  # far outside the pool: flagged, treated as masked
+    args = (m.plan, d["q"], d["kv_pool"], bad, d["kv_indptr"], d["out_cache_loc"], d["qo_indptr"],
+            d["custom_mask"], d["mask_indptr"], wl.scale, out, lse)
+    binding.run_static(*args)  # first call on this device resolves the scratch address
+    torch.cuda.synchronize()
+    assert binding.read_static_device_error() & binding.DEVERR_SLOT_RANGE
+    a0 = torch.cuda.memory_allocated()
+    f0 = torch.cuda.mem_get_info()[0]
+    for _ in range(3):
+        binding.run_static(*args)
+    torch.cuda.synchronize()
+    assert torch.cuda.memory_allocated() == a0 and torch.cuda.mem_get_info()[0] == f0
+    # each call clears the word first: a clean call reports nothing
+    binding.run_static(m.plan, d["q"], d["kv_pool"], d["kv_indices"], d["kv_indptr"], d["out_cache_loc"],
+                       d["qo_indptr"], d["custom_mask"], d["mask_indptr"], wl.scale, out, lse)
+    assert binding.read_static_device_error() == 0
 
 
 def test_static_scratch_rejects_oversized_plan():
