@@ -24,11 +24,12 @@
 //   3. the softmax warps send their partial S to the peer CTA (each warp
 //      stages its 32 rows in shared memory and issues one bulk copy that
 //      completes bytes on the peer's barrier; double-buffered, one tile
-//      ahead) as 16-bit integers with one power-of-two exponent per row and
-//      warp, i.e. per 32 values (block floating point: error <= 2^-14 of the
-//      block's largest magnitude; the distributed-shared-memory link, not the arithmetic, is
-//      what this exchange costs), add the peer's partial to their own exact
-//      one, apply the tree mask (prefix always visible, tree columns from
+//      ahead) as 16-bit integers relative to the midpoint of each block of 32
+//      values (one row of one warp), with a power-of-two step per block: the
+//      error of a partial score is at most 2^-15 (1 + 2^-10) of the block's
+//      half-range (max - min)/2, whatever the size of the scores (the distributed-shared-
+//      memory link, ~17 B/cycle per CTA, is what this exchange costs, which
+//      rules out fp32), add the peer's partial to their own exact one, apply the tree mask (prefix always visible, tree columns from
 //      custom_mask), and run the fp32 online softmax (two warps per TMEM
 //      lane quarter, 32 key columns each; "Design Decisions and
 //      Trade-Offs": mask -> -inf, streaming max/sum) with a lazily moved
@@ -103,11 +104,13 @@ constexpr uint32_t kOffStages = 0;
 constexpr uint32_t kOffQRope = kOffStages + STAGES * kStageBytes;  // rope part of Q, 64B-swizzled
 constexpr uint32_t kQRopeBytes = ROWS * 64;
 // Partial-score exchange.  One region per softmax warp: its 32 rows x NCOL
-// int16 (32 B per row, 16-byte units swizzled) followed by one int8 exponent
-// per row.  Two receive buffers (written by the peer) and two send buffers
-// (staging for the bulk copies), each NSOFT_WARPS regions.
+// int16 (16-byte units swizzled), then one int8 step exponent per row, then
+// one fp32 midpoint per row.  Two receive buffers (written by the peer) and
+// two send buffers (staging for the bulk copies), each NSOFT_WARPS regions.
 constexpr uint32_t kXRowBytes = NCOL * 2;
-constexpr uint32_t kXRegion = 32 * kXRowBytes + 32;                 // 1056
+constexpr uint32_t kXOffExp = 32 * kXRowBytes;
+constexpr uint32_t kXOffMid = kXOffExp + 32;
+constexpr uint32_t kXRegion = kXOffMid + 32 * 4;
 constexpr uint32_t kXBytes = NSOFT_WARPS * kXRegion;               // bytes completed per tile
 constexpr uint32_t kOffRx = kOffQRope + kQRopeBytes;
 constexpr uint32_t kOffTx = kOffRx + 2 * kXBytes;
@@ -116,7 +119,7 @@ constexpr uint32_t kVmaskBytes = STAGES * 8 * 8;
 constexpr uint32_t kOffRowMax = kOffVmask + kVmaskBytes;          // [2 tiles][WPQ][128 rows] f32
 constexpr uint32_t kRowMaxBytes = 2 * WPQ * ROWS * 4;
 constexpr uint32_t kOffLsum = kOffRowMax + kRowMaxBytes;          // [WPQ][128 rows] f32
-constexpr uint32_t kLsumBytes = WPQ * ROWS * 4;
+constexpr uint32_t kLsumBytes = 2 * WPQ * ROWS * 4;  // exact and bf16-rounded weight sums
 constexpr uint32_t kOffBars = kOffLsum + kLsumBytes;
 constexpr uint32_t kOffCtl = kOffBars + 256;
 constexpr uint32_t kCtlBytes = 256;
@@ -455,7 +458,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     const int64_t out_row = R.q_off * kHeads + grow;  // (token, head) row of q/out/lse
     const uint32_t qbar = bar(B_QMAX + q);            // meeting point of the WPQ warps of this quarter
     float* rowmax = reinterpret_cast<float*>(gbase + kOffRowMax);  // [tile&1][h][row]
-    float* lsum_s = reinterpret_cast<float*>(gbase + kOffLsum);    // [h][row]
+    float* lsum_s = reinterpret_cast<float*>(gbase + kOffLsum);    // [2][h][row]
     const bool tracer = (sw == 0 && lane == 0);
     const bool tracer2 = (sw == NSOFT_WARPS - 1 && lane == 0);
     // Scores stay in raw (unscaled) units; the scale enters once per element in
@@ -510,12 +513,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     // copies of tile j-1 had landed, so send buffer (j+1)&1 is free again.
     const int wreg = h * 4 + q;                               // region of this warp (same in both CTAs)
     const uint32_t x_lane = uint32_t(wreg) * kXRegion + uint32_t(lane) * kXRowBytes;
-    const uint32_t x_exp = uint32_t(wreg) * kXRegion + 32u * kXRowBytes + uint32_t(lane);
+    const uint32_t x_exp = uint32_t(wreg) * kXRegion + kXOffExp + uint32_t(lane);
+    const uint32_t x_mid = uint32_t(wreg) * kXRegion + kXOffMid + 4u * uint32_t(lane);
     // 16-byte unit swizzle: the rows sharing a 128-byte line get distinct unit orders
     const uint32_t x_sw = (uint32_t(lane) / uint32_t(128 / kXRowBytes)) & uint32_t(XU - 1);
     const uint32_t rx_peer = mapa(base + kOffRx, peer) + uint32_t(wreg) * kXRegion;
     const uint32_t peer_sx_full = mapa(bar(B_SX_FULL0), peer);  // + 8 for buffer 1
-    float m_ref = -INFINITY, l = 0.f;
+    // l: sum of the fp32 weights (gives the LSE); lr: sum of the same weights
+    // rounded to bf16 as GEMM2 multiplies them (normalises O, so that the
+    // rounding of a dominant weight cancels instead of scaling the output)
+    float m_ref = -INFINITY, l = 0.f, lr = 0.f;
     bool alive = true;
     uint32_t s[NCOL];  // this CTA's partial scores of the tile being finished
     // wind-down bookkeeping: tiles this warp sent to the peer, exchange phases
@@ -523,11 +530,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     int nsent = 0, nwaited = 0, narmed = 0;
 
     // Load tile jn's partial scores from TMEM and send them to the peer as
-    // NCOL 16-bit integers with a shared exponent k (max|v| < 2^k):
-    // u = rint(v * 2^(14-k)) + 2^15.  The rounding is done by the adder: for
-    // |y| <= 2^14, y + (1.5*2^23 + 2^15) lands in [2^23, 2^24), where the float
-    // spacing is 1, and its low 16 mantissa bits are rint(y) + 2^15.  The
-    // receiver rebuilds 1.5*2^23 + u as float bits and subtracts exactly.
+    // NCOL 16-bit integers relative to their midpoint mid = (max + min)/2 with
+    // a step 2^(k-15), where the half-range (max - min)/2 < 2^k (with a small
+    // margin): u = rint((v - mid) * 2^(15-k)) + 2^15, 31 <= u <= 2^16 - 31.
+    // The rounding is done by the adder: for |y| < 2^15, y + (1.5*2^23 + 2^15)
+    // lands in [2^23, 2^24), where the float spacing is 1, and its low 16
+    // mantissa bits are rint(y) + 2^15.  The receiver rebuilds 1.5*2^23 + u as float bits and
+    // subtracts exactly; mid travels as an fp32 per row and is added per row
+    // (in the row max and the exponent bias), never per value.
     auto fetch_and_send = [&](int jn) -> bool {
       bool ok = wait_fast(bar(B_S_FULL), jn & 1, W);
       if (!__all_sync(0xffffffffu, ok)) return false;
@@ -538,17 +548,23 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(B_S_FREE));
-      // (reductions run as four independent chains: the max instructions are opaque to the compiler)
-      float am[4] = {0.f, 0.f, 0.f, 0.f};
+      // (reductions run as independent chains: the min/max instructions are opaque to the compiler)
+      float hi[2] = {-INFINITY, -INFINITY}, lo[2] = {INFINITY, INFINITY};
 #pragma unroll
-      for (int u = 0; u < NCOL; u += 2)
-        am[(u >> 1) & 3] = max3(am[(u >> 1) & 3], fabsf(__uint_as_float(s[u])), fabsf(__uint_as_float(s[u + 1])));
-      const float amax = max3(fmaxf(am[0], am[1]), am[2], am[3]);
-      // amax in [2^(k-1), 2^k) for normal amax; 0 and subnormals give k <= -126
-      int k = int((__float_as_uint(amax) >> 23) & 0xffu) - 126;
+      for (int u = 0; u < NCOL; u += 2) {
+        hi[(u >> 1) & 1] = max3(hi[(u >> 1) & 1], __uint_as_float(s[u]), __uint_as_float(s[u + 1]));
+        lo[(u >> 1) & 1] = min3(lo[(u >> 1) & 1], __uint_as_float(s[u]), __uint_as_float(s[u + 1]));
+      }
+      const float vmax = fmaxf(hi[0], hi[1]), vmin = fminf(lo[0], lo[1]);
+      const float mid = 0.5f * (vmax + vmin);
+      // bound on |v - mid| over the block, with a 2^-10 margin for the roundings
+      // of mid and of the subtractions: |y| = |v - mid| * 2^(15-k) < 2^15 - 31
+      const float span = fmaxf(vmax - mid, mid - vmin) * (1.0f + 0x1p-10f);
+      // span in [2^(k-1), 2^k) for normal span; 0 and subnormals give k <= -126
+      int k = int((__float_as_uint(span) >> 23) & 0xffu) - 126;
       k = max(-100, min(k, 100));
-      const float qs = __int_as_float((127 + 14 - k) << 23);  // 2^(14-k), exact
-      const uint64_t qs2 = f2_pack(qs, qs), mg2 = f2_pack(kQuantMagic, kQuantMagic);
+      const float qs = __int_as_float((127 + 15 - k) << 23);  // 2^(15-k), exact
+      const uint64_t qs2 = f2_pack(qs, qs), mg2 = f2_pack(kQuantMagic, kQuantMagic), nmid2 = f2_pack(-mid, -mid);
       const uint32_t tx = base + kOffTx + uint32_t(jn & 1) * kXBytes;
 #pragma unroll
       for (int u = 0; u < XU; ++u) {
@@ -557,11 +573,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         for (int e = 0; e < 4; ++e) {
           const int c0 = 8 * u + 2 * e;
           float a, b;
-          f2_unpack(f2_fma(f2_pack(__uint_as_float(s[c0]), __uint_as_float(s[c0 + 1])), qs2, mg2), a, b);
+          // v - mid is exact to 2^-24 of the half-range; the fma then rounds to the step
+          const uint64_t d2 = f2_add(f2_pack(__uint_as_float(s[c0]), __uint_as_float(s[c0 + 1])), nmid2);
+          f2_unpack(f2_fma(d2, qs2, mg2), a, b);
           w[e] = __byte_perm(__float_as_uint(a), __float_as_uint(b), 0x5410);
         }
         st_shared_v4(tx + x_lane + ((uint32_t(u) ^ x_sw) << 4), w[0], w[1], w[2], w[3]);
       }
+      st_shared_f32(tx + x_mid, mid);
       st_shared_u8(tx + x_exp, uint32_t(k));
       fence_proxy_async_smem();  // the bulk copy reads the staging through the async proxy
       __syncwarp();
@@ -588,11 +607,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       nwaited = j + 1;
       if (tracer) MTV_TR(2, j, 2);
       if (tracer2) MTV_TR(3, j, 2);
-      float x[NCOL];  // full scores of this warp's columns: own exact partial + peer's
+      // full scores of this warp's columns, less the peer's block midpoint xmid:
+      // own exact partial + peer's partial relative to xmid
+      float x[NCOL], xmid;
       {
         const unsigned char* rxb = gbase + kOffRx + (j & 1) * kXBytes;
         const int kp = *reinterpret_cast<const signed char*>(rxb + x_exp);
-        const float dq = __int_as_float((127 - 14 + kp) << 23);  // 2^(k-14)
+        xmid = *reinterpret_cast<const float*>(rxb + x_mid);
+        const float dq = __int_as_float((127 - 15 + kp) << 23);  // 2^(k-15)
         const uint64_t dq2 = f2_pack(dq, dq), nmg2 = f2_pack(-kQuantMagic, -kQuantMagic);
         const uint4* row = reinterpret_cast<const uint4*>(rxb + x_lane);
 #pragma unroll
@@ -646,7 +668,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int cc = 0; cc < NCOL; cc += 2) mx[(cc >> 1) & 3] = max3(mx[(cc >> 1) & 3], x[cc], x[cc + 1]);
-      float mt = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]);
+      float mt = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) + xmid;  // -inf stays -inf
       rowmax[((j & 1) * WPQ + h) * ROWS + rr] = mt;
       if (tracer) MTV_TR(2, j, 9);
       if (tracer2) MTV_TR(3, j, 9);
@@ -665,27 +687,32 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       const float fac = move ? ex2((m_ref - m_new) * c) : 1.f;  // ex2(-inf) = 0
       if (move) {
         l *= fac;
+        lr *= fac;
         m_ref = m_new;
       }
-      const float nb = (m_ref == -INFINITY) ? 0.f : -m_ref * c;
+      // exponent c*(x + xmid - m_ref): the midpoint enters through the bias
+      const float nb = (m_ref == -INFINITY) ? 0.f : (xmid - m_ref) * c;
       const uint64_t c2 = f2_pack(c, c), nb2 = f2_pack(nb, nb);
-      uint64_t ls[4];
+      uint64_t ls[2], lsr[2];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) ls[i] = f2_pack(0.f, 0.f);
+      for (int i = 0; i < 2; ++i) ls[i] = lsr[i] = f2_pack(0.f, 0.f);
       uint32_t pk[NCOL / 2];
 #pragma unroll
       for (int u = 0; u < NCOL / 2; ++u) {
         float e0, e1;
         f2_unpack(f2_fma(f2_pack(x[2 * u], x[2 * u + 1]), c2, nb2), e0, e1);
         const float p0 = ex2(e0), p1 = ex2(e1);
-        ls[u & 3] = f2_add(ls[u & 3], f2_pack(p0, p1));
-        const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);
+        ls[u & 1] = f2_add(ls[u & 1], f2_pack(p0, p1));
+        const __nv_bfloat162 b = __floats2bfloat162_rn(p0, p1);  // p0 in the low half
         pk[u] = *reinterpret_cast<const uint32_t*>(&b);
+        lsr[u & 1] = f2_add(lsr[u & 1], f2_pack(__uint_as_float(pk[u] << 16), __uint_as_float(pk[u] & 0xffff0000u)));
       }
       {
-        float a0, a1;
-        f2_unpack(f2_add(f2_add(ls[0], ls[1]), f2_add(ls[2], ls[3])), a0, a1);
-        l += a0 + a1;  // unrounded weights normalise O and give the LSE
+        float a0, a1, b0, b1;
+        f2_unpack(f2_add(ls[0], ls[1]), a0, a1);
+        f2_unpack(f2_add(lsr[0], lsr[1]), b0, b1);
+        l += a0 + a1;
+        lr += b0 + b1;
       }
 
       if (tracer) MTV_TR(2, j, 10);
@@ -727,17 +754,21 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     // the row's WPQ partial sums meet in shared memory
     if (alive) {
       lsum_s[h * ROWS + rr] = l;
+      lsum_s[(WPQ + h) * ROWS + rr] = lr;
       __syncwarp();
       if (lane == 0) mbar_arrive(qbar);
       bool ok = wait_fast(qbar, T & 1, W);
       alive = __all_sync(0xffffffffu, ok);
     }
     if (alive) {
-      float tot = 0.f;
+      float tot = 0.f, totr = 0.f;
 #pragma unroll
-      for (int hh = 0; hh < WPQ; ++hh) tot += lsum_s[hh * ROWS + rr];
+      for (int hh = 0; hh < WPQ; ++hh) {
+        tot += lsum_s[hh * ROWS + rr];
+        totr += lsum_s[(WPQ + hh) * ROWS + rr];
+      }
       tc_fence_after();
-      const float inv = tot > 0.f ? 1.f / tot : 0.f;
+      const float inv = totr > 0.f ? 1.f / totr : 0.f;
       // Normalised O columns go through shared memory so that the global
       // stores are row-contiguous: each thread holds one row, but a warp
       // stores two rows x 256 bytes per instruction.  The staging uses the

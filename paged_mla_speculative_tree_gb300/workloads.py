@@ -301,6 +301,39 @@ def shared_prefix(bs: int = 16, prefix: int = 32768, tree: int = 1, num_slots: i
                     meta={"shared_prefix": True})
 
 
+# ----------------------------------------------------------------------------
+# large-logit variants (input transforms; the values stay exact bf16)
+# ----------------------------------------------------------------------------
+
+def scaled_q(wl: Workload, alpha: float) -> Workload:
+    """q multiplied by ``alpha`` and rounded to bf16 again: scaled logits grow
+    by alpha (alpha ~4.5 puts the largest logits of the N(0,1) workloads near
+    30, where attention in trained models routinely sits)."""
+    wl.q = (wl.q.float() * alpha).to(torch.bfloat16)
+    wl.name += f"_qx{alpha:g}"
+    wl.meta["q_scale"] = alpha
+    return wl
+
+
+def common_component(wl: Workload, a: float = 1.7, b: float = 2.0, seed: int = 7) -> Workload:
+    """Every latent row of the pool gets ``a * u`` and every query ``b * u``
+    added in the 512 latent dims, u a seeded +-1 vector: all scores share an
+    offset of a*b*512 raw units (a*b*256 ~ 870 in each half of the latent
+    dims) on top of their N(0,1)-driven spread -- keys that share a large
+    common direction, as the latent rows of trained models do."""
+    g = torch.Generator().manual_seed(seed)
+    u = torch.where(torch.rand(D_LATENT, generator=g) < 0.5, -1.0, 1.0)
+    pool = wl.kv_pool.float()
+    pool[:, :D_LATENT] += a * u
+    wl.kv_pool = pool.to(torch.bfloat16)
+    q = wl.q.float()
+    q[:, :, :D_LATENT] += b * u
+    wl.q = q.to(torch.bfloat16)
+    wl.name += "_common"
+    wl.meta["common_component"] = (a, b)
+    return wl
+
+
 def custom(prefix_lens, parents, num_slots, seed, contiguous=False,
            mask_layout=MASK_FULL_ROW, name="custom") -> Workload:
     """Any shape: used by the tests for ragged and degenerate cases."""

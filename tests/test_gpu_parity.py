@@ -206,6 +206,29 @@ def test_named_workload_sampled(flags, name):
     assert np.all(np.isfinite(lse)) and np.all(np.isfinite(out))
 
 
+@pytest.mark.parametrize("name", ["batch4", "long_random"])
+def test_large_logits_sampled(flags, name):
+    """q scaled by 4.5: the largest scaled logits reach ~30 and one CTA's
+    partial scores reach a few hundred raw units, where a score exchange whose
+    error grows with the size of the scores would miss the LSE tolerance."""
+    wl = W.scaled_q(W.WORKLOADS[name](), 4.5)
+    out, lse = G.run_gpu(wl, flags)
+    rows = G.sample_rows(wl, 160, seed=hash(name) % 997)
+    _, ref_lse = oracle.mla_tree_verify(wl, rows=rows)
+    assert ref_lse.max() > 25.0  # the regime this test is about
+    G.compare(wl, out, lse, rows=rows, tag=f"{name} large logits")
+
+
+@pytest.mark.parametrize("name", ["batch4", "long_random"])
+def test_large_common_component_sampled(flags, name):
+    """Keys and queries sharing one large latent direction: every score carries
+    an offset of ~1,740 raw units (~870 in each CTA's half of the dims)."""
+    wl = W.common_component(W.WORKLOADS[name]())
+    out, lse = G.run_gpu(wl, flags)
+    rows = G.sample_rows(wl, 160, seed=hash(name) % 991)
+    G.compare(wl, out, lse, rows=rows, tag=f"{name} common component")
+
+
 def test_long_contiguous_equals_random_slots(flags):
     a, b = W.long_context(True), W.long_context(False)
     oa, la = G.run_gpu(a, flags)
