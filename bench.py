@@ -2,11 +2,18 @@
 """Benchmark of MLA tree-verify attention on GB300 (one JSON line on stdout).
 
 A step is one verify-attention call (partial kernel + split-K combine) over the
-4-request short-context workload (prefix 5,760, 16-node trees, 65,536-slot
-pool) unless --workload says otherwise.  Timing: CUDA events on the launching
-stream around each call, L2 flushed (256 MiB write) between calls outside the
-events, W untimed warm-up calls, K timed calls bracketed by barrier +
-synchronize.  ``value`` is microseconds per call for the whole job.
+capture-safe stress workload (16 requests x 131,072-token prefix x 64-node
+tree on a 2.2M-slot pool), captured once into a CUDA graph and replayed every
+step, unless --workload says otherwise (the other workloads are timed as
+direct calls).  Timing: CUDA events on the launching stream around each step,
+L2 flushed (256 MiB write) between steps outside the events, W untimed
+warm-up steps, K timed steps bracketed by barrier + synchronize.  ``value`` is
+microseconds per call of the whole batch.  The roofline block times the
+dominant kernel (the split-K partial kernel) alone, launched through
+mla_tree_verify_run_steps with CUDA events on its stream.  With N GPUs (torchrun)
+the batch's requests are partitioned over the ranks (balanced on
+(p_r + n_r) * n_r; requests are independent, so no collective touches the data
+path) and ``value`` is the slowest rank's time per call of the whole batch.
 
 --impl reference times the CPU oracle (the only other implementation of this
 path) on the host cores on a bounded row sample of the same workload and
@@ -35,11 +42,13 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 from paged_mla_speculative_tree_gb300 import binding  # noqa: E402
+from paged_mla_speculative_tree_gb300 import partition as PT  # noqa: E402
 from paged_mla_speculative_tree_gb300 import workloads as W  # noqa: E402
 
 METRIC = "verify-attn µs/call, effective HBM GB/s, % of roofline (1×GB300)"
 UNIT = "us/call"
-DEFAULT_WORKLOAD = "batch4"
+DEFAULT_WORKLOAD = "stress"
+GRAPH_WORKLOADS = {"stress"}  # timed as replays of the captured call
 
 
 def load_peaks():
@@ -53,17 +62,12 @@ def load_peaks():
 
 
 def max_over_ranks(ms, ws, dev=None):
-    """The slowest rank's time: every replica runs the same call concurrently."""
+    """The slowest rank's time: the ranks run their shares of the batch concurrently."""
     if ws <= 1:
         return ms
     t = torch.tensor([ms], dtype=torch.float64, device=dev)
     torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
     return float(t.item())
-
-
-def job_us_per_call(ms, ws):
-    """Whole-job microseconds per call: ws replicas finish ws calls in ``ms``."""
-    return ms * 1e3 / ws
 
 
 def dist_env():
@@ -242,10 +246,19 @@ def run_ours(args):
         dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    wl = make_workload(args.workload)
+    full = make_workload(args.workload)
+    if ws > 1:
+        # requests are independent: each rank runs its share of the batch
+        # (balanced on (p_r + n_r) * n_r), no exchange on the data path
+        parts = PT.partition_requests(full.prefix_lens, full.tree_sizes, ws)
+        wl = W.sub_workload(full, parts[rank])
+    else:
+        parts = [list(range(full.bs))]
+        wl = full
     d = device_inputs(wl, dev)
-    out = torch.empty((wl.total_q, 64, 512), dtype=torch.bfloat16, device=dev)
-    lse = torch.empty((wl.total_q, 64), dtype=torch.float32, device=dev)
+    T = max(wl.total_q, 1)
+    out = torch.empty((T, 64, 512), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((T, 64), dtype=torch.float32, device=dev)
     # For the end-to-end steps, the per-step inputs (q and the metadata) live in
     # one packed device buffer and the outputs in another, so that a step from
     # host memory is one copy in and one copy out (the pool stays in HBM).
@@ -254,26 +267,43 @@ def run_ours(args):
         in_host_views[k].copy_(wl_tensor(wl, k))
     d_e2e = dict(d, **in_views)
     out_dev, out_views, out_host, _, d2h = packed_buffers(
-        {"out": torch.empty((wl.total_q, 64, 512), dtype=torch.bfloat16),
-         "lse": torch.empty((wl.total_q, 64), dtype=torch.float32)}, dev)
+        {"out": torch.empty((T, 64, 512), dtype=torch.bfloat16),
+         "lse": torch.empty((T, 64), dtype=torch.float32)}, dev)
     flags = binding.FLAG_SIMT_FLOOR if args.simt else 0
-    m = binding.MlaTreeVerify(wl.bs, wl.max_q_per_req, wl.total_q, wl.max_prefix, device=local,
+    m = binding.MlaTreeVerify(wl.bs, wl.max_q_per_req, T, wl.max_prefix, device=local,
                               mask_layout=wl.mask_layout, flags=flags, nsplit=args.nsplit)
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
-    def call():
-        m(d["q"], d["kv_pool"], d["kv_indices"], d["kv_indptr"], d["out_cache_loc"], d["qo_indptr"],
-          d["custom_mask"], d["mask_indptr"], wl.scale, out, lse)
+    def call(steps=None):
+        binding.run(m.plan, d["q"], d["kv_pool"], d["kv_indices"], d["kv_indptr"], d["out_cache_loc"],
+                    d["qo_indptr"], d["custom_mask"], d["mask_indptr"], wl.scale, out, lse, m.workspace,
+                    steps=steps)
 
     def call_e2e():
         m(d_e2e["q"], d_e2e["kv_pool"], d_e2e["kv_indices"], d_e2e["kv_indptr"], d_e2e["out_cache_loc"],
           d_e2e["qo_indptr"], d_e2e["custom_mask"], d_e2e["mask_indptr"], wl.scale, out_views["out"],
           out_views["lse"])
 
+    use_graph = args.graph if args.graph is not None else (args.workload in GRAPH_WORKLOADS)
+    step = call
+    if use_graph:
+        # captured once with static buffers, replayed every step (the capture-safe use of the call)
+        side = torch.cuda.Stream()
+        side.wait_stream(stream)
+        with torch.cuda.stream(side):
+            call()
+        stream.wait_stream(side)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            call()
+        torch.cuda.synchronize()
+        step = graph.replay
+
     for _ in range(args.warmup):
         flush.fill_(1)
-        call()
+        step()
     torch.cuda.synchronize()
     assert m.device_error() == 0, "device error word set during warm-up"
 
@@ -287,7 +317,7 @@ def run_ours(args):
         for k in range(args.steps):
             flush.fill_(k & 0xff)
             starts[k].record(stream)
-            call()
+            step()
             ends[k].record(stream)
             if k % 2 == 1:
                 clk.sample()  # host-side, between launches: the GPU is still busy with the queued steps
@@ -295,10 +325,24 @@ def run_ours(args):
         if ws > 1:
             torch.distributed.barrier()
         wall = time.perf_counter() - t_wall
-    per_call_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    per_call_ms = [s_.elapsed_time(e) for s_, e in zip(starts, ends)]
     ms = max_over_ranks(float(np.mean(per_call_ms)), ws, dev)
     clocks = clk.summary()
-    launches_per_call = 1 + (1 if m.plan.nsplit > 1 else 0)
+    launches_per_call = (1 + (1 if m.plan.nsplit > 1 else 0)) if wl.bs else 0
+
+    # the dominant kernel alone: the partial (split-K) launch, CUDA events on its stream
+    for _ in range(max(1, args.warmup // 2)):
+        flush.fill_(1)
+        call(binding.STEP_PARTIAL)
+    p_s = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    p_e = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for k in range(args.steps):
+        flush.fill_(k & 0xff)
+        p_s[k].record(stream)
+        call(binding.STEP_PARTIAL)
+        p_e[k].record(stream)
+    torch.cuda.synchronize()
+    partial_ms = max_over_ranks(float(np.mean([a.elapsed_time(b) for a, b in zip(p_s, p_e)])), ws, dev)
 
     # end to end through the public API with host buffers (pinned), copies inside the timed region
     for _ in range(max(1, args.warmup)):
@@ -312,48 +356,66 @@ def run_ours(args):
         e2e_step(in_host, in_dev, call_e2e, out_dev, out_host)
         e_e[k].record(stream)
     torch.cuda.synchronize()
-    e2e_ms = max_over_ranks(float(np.mean([s.elapsed_time(e) for s, e in zip(e_s, e_e)])), ws, dev)
+    e2e_ms = max_over_ranks(float(np.mean([s_.elapsed_time(e) for s_, e in zip(e_s, e_e)])), ws, dev)
+    assert m.device_error() == 0, "device error word set during the timed runs"
 
     if rank != 0:
         if ws > 1:
             torch.distributed.destroy_process_group()
         return 0
     peaks = load_peaks()
-    flops = wl.algorithmic_flops()
-    nbytes = wl.algorithmic_bytes()
+    # whole-job figures: the full batch (all ranks' requests) per step
+    flops = full.algorithmic_flops()
+    nbytes = full.algorithmic_bytes()
     achieved_tf = flops / (ms * 1e-3) / 1e12
     achieved_gbs = nbytes / (ms * 1e-3) / 1e9
     peak_tf = peaks["bf16_tflops"]
     roof_ms = max(nbytes / (peaks["hbm_gbs"] * 1e9), flops / (peak_tf * 1e12)) * 1e3
     bound = "tensor" if flops / (peak_tf * 1e12) >= nbytes / (peaks["hbm_gbs"] * 1e9) else "hbm"
+    # the dominant kernel on this rank's share (rank 0's launch)
+    k_flops, k_bytes = wl.algorithmic_flops(), wl.algorithmic_bytes()
+    k_tf = k_flops / (partial_ms * 1e-3) / 1e12 if partial_ms > 0 else 0.0
+    k_gbs = k_bytes / (partial_ms * 1e-3) / 1e9 if partial_ms > 0 else 0.0
     traffic = load_traffic(wl.name, m.plan)
+    kernel_name = "partial_simt_kernel" if args.simt else "partial_tc_kernel"
     if bound == "tensor":
-        roof = {"bound": "tensor", "achieved": achieved_tf, "peak": peak_tf, "unit": "TFLOP/s",
-                "frac": achieved_tf / peak_tf, "traffic": traffic}
+        roof = {"bound": "tensor", "achieved": k_tf, "peak": peak_tf, "unit": "TFLOP/s", "frac": k_tf / peak_tf,
+                "traffic": traffic}
     else:
-        roof = {"bound": "hbm", "achieved": achieved_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved_gbs / peaks["hbm_gbs"], "traffic": traffic}
-    roof.update({"peak_source": peaks["source"] + (" burst" if bound == "tensor" else ""),
-                 "timed": "whole call (partial + combine), CUDA events on the launch stream",
-                 "roofline_us": roof_ms * 1e3, "frac_of_roofline": roof_ms / ms,
-                 "effective_hbm_gbs": achieved_gbs})
+        roof = {"bound": "hbm", "achieved": k_gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": k_gbs / peaks["hbm_gbs"], "traffic": traffic}
+    roof.update({
+        "kernel": kernel_name, "kernel_us": partial_ms * 1e3,
+        "peak_source": peaks["source"] + (" burst" if bound == "tensor" else ""),
+        "frac_of_sustained": k_tf / peaks["bf16_tflops_sustained"] if bound == "tensor" else None,
+        "timed": "the partial kernel alone (run_steps PARTIAL), CUDA events on its launch stream, "
+                 f"{args.steps} launches, L2 flushed between",
+        "algorithmic_flops_per_launch": k_flops, "algorithmic_bytes_per_launch": k_bytes,
+        "whole_call": {"achieved_tflops": achieved_tf, "frac": achieved_tf / peak_tf if bound == "tensor" else
+                       achieved_gbs / peaks["hbm_gbs"], "roofline_us": roof_ms * 1e3,
+                       "frac_of_roofline": roof_ms / ms, "effective_hbm_gbs": achieved_gbs}})
     line = {
-        "metric": METRIC, "value": job_us_per_call(ms, ws), "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False, "scaling": "weak",
+        "metric": METRIC, "value": ms * 1e3, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": False,
+        "scaling": "strong" if ws > 1 else "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "bs": wl.bs, "prefix": wl.prefix_lens, "tree": wl.tree_sizes,
-                   "num_slots": wl.num_slots, "heads": 64, "d_qk": 576, "d_v": 512,
+        "config": {"workload": full.name, "bs": full.bs, "prefix": full.prefix_lens, "tree": full.tree_sizes,
+                   "num_slots": full.num_slots, "heads": 64, "d_qk": 576, "d_v": 512,
                    "kernel": "simt-floor" if args.simt else "tcgen05", "nsplit": int(m.plan.nsplit),
-                   "split_keys": int(m.plan.split_keys), "parallelism": f"replicas x{ws}",
-                   "l2": "flushed between calls (256 MiB write outside the timed events)"},
+                   "split_keys": int(m.plan.split_keys),
+                   "parallelism": f"requests partitioned over {ws} GPUs" if ws > 1 else "1 GPU",
+                   "requests_per_rank": [len(p_) for p_ in parts],
+                   "timing": "CUDA-graph replay of the captured call" if use_graph else "direct calls",
+                   "l2": "flushed between calls (256 MiB write outside the timed events); the inputs "
+                         + ("also exceed L2" if full.algorithmic_bytes() > 129e6 else "fit in L2")},
         "effective_hbm_gbs": achieved_gbs, "achieved_tflops": achieved_tf,
         "roofline": roof, "clocks": clocks, "gpu_launches": launches_per_call * args.steps,
-        "e2e": {"value": job_us_per_call(e2e_ms, ws), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": e2e_ms * 1e3, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "wall_s_timed_region": wall,
     }
-    if not args.no_cpu_baseline:
-        us, cores, sample = cpu_oracle_timing(wl, target_s=args.cpu_seconds)
+    if not args.no_cpu_baseline and ws == 1:
+        us, cores, sample = cpu_oracle_timing(full, target_s=args.cpu_seconds)
         line["cpu_baseline"] = {"value": us, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": sample}
     print(json.dumps(line), flush=True)
     if ws > 1:
@@ -701,6 +763,9 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--nsplit", type=int, default=0)
     ap.add_argument("--simt", action="store_true", help="time the SIMT correctness-floor kernel")
+    ap.add_argument("--graph", dest="graph", action="store_true", default=None,
+                    help="time replays of a captured CUDA graph (default for stress)")
+    ap.add_argument("--no-graph", dest="graph", action="store_false")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--op", choices=["verify", "mask", "accept", "defrag", "shared"], default="verify",

@@ -178,6 +178,29 @@ int mla_tree_verify_run(const mtv_plan_t* plan, const void* q, const void* kv_po
                         const int64_t* mask_indptr, float scale, void* out, float* lse,
                         void* workspace, uint64_t workspace_bytes, void* stream);
 
+/* Steps of one pass, for mla_tree_verify_run_steps. */
+#define MTV_STEP_PARTIAL 0x1   /* the split-K partial kernel (writes out/lse itself with one split) */
+#define MTV_STEP_COMBINE 0x2   /* the combine of the splits (nothing to do with one split)         */
+
+/*
+ * mla_tree_verify_run_steps -- mla_tree_verify_run split into its launches,
+ * so that a caller (a profiler, a benchmark) can enqueue work such as CUDA
+ * events between them.  `steps` is MTV_STEP_PARTIAL, MTV_STEP_COMBINE or both
+ * (both is exactly mla_tree_verify_run).  MTV_STEP_PARTIAL followed by
+ * MTV_STEP_COMBINE on the same stream with the same arguments gives the same
+ * result as one mla_tree_verify_run, bit for bit; the combine launched alone
+ * is an ordinary stream successor instead of a programmatic dependent of the
+ * partial kernel.  Same arguments, checks and errors as mla_tree_verify_run;
+ * MTV_E_BAD_ARGUMENT for an empty or unknown step mask.
+ */
+int mla_tree_verify_run_steps(const mtv_plan_t* plan, const void* q, const void* kv_pool,
+                              int64_t num_slots, const int64_t* kv_indices, int64_t kv_indices_len,
+                              const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                              int64_t out_cache_loc_len, const int64_t* qo_indptr,
+                              const uint8_t* custom_mask, int64_t custom_mask_len,
+                              const int64_t* mask_indptr, float scale, void* out, float* lse,
+                              void* workspace, uint64_t workspace_bytes, int steps, void* stream);
+
 /* Text for a return code (static storage; never NULL). */
 const char* mla_tree_verify_strerror(int code);
 

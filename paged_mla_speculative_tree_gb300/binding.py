@@ -17,6 +17,8 @@ MASK_FULL_ROW = 0
 MASK_TREE_ONLY = 1
 FLAG_SIMT_FLOOR = 0x1
 FLAG_TEST_SHORT_WAITS = 0x100  # test only: pipeline waits give up at once (timeout path)
+STEP_PARTIAL = 0x1
+STEP_COMBINE = 0x2
 DEVERR_SLOT_RANGE = 0x1
 DEVERR_INDPTR = 0x2
 DEVERR_TIMEOUT = 0x4
@@ -52,7 +54,7 @@ class MtvError(RuntimeError):
 
 
 _lib = None
-SYMBOLS = ("mla_tree_verify_plan", "mla_tree_verify_run", "mla_tree_verify_strerror",
+SYMBOLS = ("mla_tree_verify_plan", "mla_tree_verify_run", "mla_tree_verify_run_steps", "mla_tree_verify_strerror",
            "mla_tree_verify_clear_device_error", "mla_tree_verify_read_device_error",
            "mla_tree_verify_run_static", "mla_tree_verify_read_static_device_error", "mla_tree_mask_build", "mla_tree_accept", "mla_kv_defrag",
            "mla_tree_group_prefix")
@@ -78,6 +80,9 @@ def load(path: str | None = None):
     lib.mla_tree_verify_run.argtypes = [ctypes.POINTER(MtvPlan), P, P, I64, P, I64, P, P, I64, P, P, I64, P,
                                         ctypes.c_float, P, P, P, U64, P]
     lib.mla_tree_verify_run.restype = I32
+    lib.mla_tree_verify_run_steps.argtypes = [ctypes.POINTER(MtvPlan), P, P, I64, P, I64, P, P, I64, P, P, I64, P,
+                                              ctypes.c_float, P, P, P, U64, I32, P]
+    lib.mla_tree_verify_run_steps.restype = I32
     lib.mla_tree_verify_strerror.argtypes = [I32]
     lib.mla_tree_verify_strerror.restype = ctypes.c_char_p
     lib.mla_tree_verify_clear_device_error.argtypes = [P, P]
@@ -158,23 +163,29 @@ def _numel(t, given):
 
 def run(p: MtvPlan, q, kv_pool, kv_indices, kv_indptr, out_cache_loc, qo_indptr, custom_mask,
         mask_indptr, scale: float, out, lse, workspace, stream=None, check: bool = True,
-        kv_indices_len=None, out_cache_loc_len=None, custom_mask_len=None) -> int:
-    """Enqueues one verify-attention pass; returns the ABI code (raises if check).
-    Buffer lengths default to the tensors' element counts."""
+        kv_indices_len=None, out_cache_loc_len=None, custom_mask_len=None, steps=None) -> int:
+    """Enqueues one verify-attention pass (or, with ``steps``, only the given
+    launches of it); returns the ABI code (raises if check).  Buffer lengths
+    default to the tensors' element counts."""
     num_slots = kv_pool.shape[0] if isinstance(kv_pool, torch.Tensor) else 0
     ws_bytes = workspace.numel() * workspace.element_size() if isinstance(workspace, torch.Tensor) else 0
     wsp = _ptr(workspace, torch.uint8, "workspace")
-    rc = load().mla_tree_verify_run(
-        ctypes.byref(p), _ptr(q, torch.bfloat16, "q", wsp), _ptr(kv_pool, torch.bfloat16, "kv_pool", wsp),
-        int(num_slots), _ptr(kv_indices, torch.int64, "kv_indices", wsp), _numel(kv_indices, kv_indices_len),
-        _ptr(kv_indptr, torch.int32, "kv_indptr"), _ptr(out_cache_loc, torch.int64, "out_cache_loc", wsp),
-        _numel(out_cache_loc, out_cache_loc_len), _ptr(qo_indptr, torch.int64, "qo_indptr"),
-        _ptr(custom_mask, torch.uint8, "custom_mask", wsp), _numel(custom_mask, custom_mask_len),
-        _ptr(mask_indptr, torch.int64, "mask_indptr"), float(scale),
-        _ptr(out, torch.bfloat16, "out", wsp), _ptr(lse, torch.float32, "lse", wsp),
-        wsp, int(ws_bytes), _stream_handle(stream))
+    args = (ctypes.byref(p), _ptr(q, torch.bfloat16, "q", wsp), _ptr(kv_pool, torch.bfloat16, "kv_pool", wsp),
+            int(num_slots), _ptr(kv_indices, torch.int64, "kv_indices", wsp), _numel(kv_indices, kv_indices_len),
+            _ptr(kv_indptr, torch.int32, "kv_indptr"), _ptr(out_cache_loc, torch.int64, "out_cache_loc", wsp),
+            _numel(out_cache_loc, out_cache_loc_len), _ptr(qo_indptr, torch.int64, "qo_indptr"),
+            _ptr(custom_mask, torch.uint8, "custom_mask", wsp), _numel(custom_mask, custom_mask_len),
+            _ptr(mask_indptr, torch.int64, "mask_indptr"), float(scale),
+            _ptr(out, torch.bfloat16, "out", wsp), _ptr(lse, torch.float32, "lse", wsp),
+            wsp, int(ws_bytes))
+    if steps is None:
+        rc = load().mla_tree_verify_run(*args, _stream_handle(stream))
+        what = "mla_tree_verify_run"
+    else:
+        rc = load().mla_tree_verify_run_steps(*args, int(steps), _stream_handle(stream))
+        what = "mla_tree_verify_run_steps"
     if check and rc != MTV_OK:
-        raise MtvError(rc, "mla_tree_verify_run")
+        raise MtvError(rc, what)
     return rc
 
 

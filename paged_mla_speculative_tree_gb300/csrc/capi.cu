@@ -141,13 +141,16 @@ int mla_tree_verify_plan(int device, int bs, int max_q_per_req, int64_t total_q_
   return MTV_OK;
 }
 
-int mla_tree_verify_run(const mtv_plan_t* plan, const void* q, const void* kv_pool,
-                        int64_t num_slots, const int64_t* kv_indices, int64_t kv_indices_len,
-                        const int32_t* kv_indptr, const int64_t* out_cache_loc,
-                        int64_t out_cache_loc_len, const int64_t* qo_indptr,
-                        const uint8_t* custom_mask, int64_t custom_mask_len,
-                        const int64_t* mask_indptr, float scale, void* out, float* lse,
-                        void* workspace, uint64_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+// Host checks and kernel launches shared by run and run_steps.
+static int run_impl(const mtv_plan_t* plan, const void* q, const void* kv_pool, int64_t num_slots,
+                    const int64_t* kv_indices, int64_t kv_indices_len, const int32_t* kv_indptr,
+                    const int64_t* out_cache_loc, int64_t out_cache_loc_len, const int64_t* qo_indptr,
+                    const uint8_t* custom_mask, int64_t custom_mask_len, const int64_t* mask_indptr,
+                    float scale, void* out, float* lse, void* workspace, uint64_t workspace_bytes,
+                    int steps, void* stream) {
+  if ((steps & ~(MTV_STEP_PARTIAL | MTV_STEP_COMBINE)) || steps == 0) return MTV_E_BAD_ARGUMENT;
   if (!plan) return MTV_E_NULL_POINTER;
   if (plan->magic != MTV_PLAN_MAGIC || plan->version != MTV_ABI_VERSION) return MTV_E_BAD_PLAN;
   if (!workspace || !kv_indptr || !qo_indptr || !mask_indptr) return MTV_E_NULL_POINTER;
@@ -204,11 +207,41 @@ int mla_tree_verify_run(const mtv_plan_t* plan, const void* q, const void* kv_po
   P.wait_cycles = (plan->flags & MTV_FLAG_TEST_SHORT_WAITS) ? 0ll : (1ll << 31);
 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  cudaError_t e = (plan->flags & MTV_FLAG_SIMT_FLOOR) ? launch_partial_simt(P, st)
-                                                      : launch_partial_tc(P, st);
-  if (e == cudaSuccess && plan->nsplit > 1) e = launch_combine(P, st);
+  cudaError_t e = cudaSuccess;
+  if (steps & MTV_STEP_PARTIAL)
+    e = (plan->flags & MTV_FLAG_SIMT_FLOOR) ? launch_partial_simt(P, st) : launch_partial_tc(P, st);
+  // Launched right behind the partial kernel, the combine is its programmatic
+  // dependent; launched alone it waits for the stream's earlier work as usual.
+  if (e == cudaSuccess && plan->nsplit > 1 && (steps & MTV_STEP_COMBINE))
+    e = launch_combine(P, st, (steps & MTV_STEP_PARTIAL) != 0);
   if (e != cudaSuccess) return MTV_E_CUDA;
   return MTV_OK;
+}
+
+extern "C" {
+
+int mla_tree_verify_run(const mtv_plan_t* plan, const void* q, const void* kv_pool,
+                        int64_t num_slots, const int64_t* kv_indices, int64_t kv_indices_len,
+                        const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                        int64_t out_cache_loc_len, const int64_t* qo_indptr,
+                        const uint8_t* custom_mask, int64_t custom_mask_len,
+                        const int64_t* mask_indptr, float scale, void* out, float* lse,
+                        void* workspace, uint64_t workspace_bytes, void* stream) {
+  return run_impl(plan, q, kv_pool, num_slots, kv_indices, kv_indices_len, kv_indptr, out_cache_loc,
+                  out_cache_loc_len, qo_indptr, custom_mask, custom_mask_len, mask_indptr, scale, out, lse,
+                  workspace, workspace_bytes, MTV_STEP_PARTIAL | MTV_STEP_COMBINE, stream);
+}
+
+int mla_tree_verify_run_steps(const mtv_plan_t* plan, const void* q, const void* kv_pool,
+                              int64_t num_slots, const int64_t* kv_indices, int64_t kv_indices_len,
+                              const int32_t* kv_indptr, const int64_t* out_cache_loc,
+                              int64_t out_cache_loc_len, const int64_t* qo_indptr,
+                              const uint8_t* custom_mask, int64_t custom_mask_len,
+                              const int64_t* mask_indptr, float scale, void* out, float* lse,
+                              void* workspace, uint64_t workspace_bytes, int steps, void* stream) {
+  return run_impl(plan, q, kv_pool, num_slots, kv_indices, kv_indices_len, kv_indptr, out_cache_loc,
+                  out_cache_loc_len, qo_indptr, custom_mask, custom_mask_len, mask_indptr, scale, out, lse,
+                  workspace, workspace_bytes, steps, stream);
 }
 
 int mla_tree_verify_clear_device_error(void* workspace, void* stream) {

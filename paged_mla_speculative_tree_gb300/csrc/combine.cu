@@ -99,7 +99,7 @@ __global__ void __launch_bounds__(kThreads) combine_kernel(const Params P) {
 
 }  // namespace
 
-cudaError_t launch_combine(const Params& P, cudaStream_t st) {
+cudaError_t launch_combine(const Params& P, cudaStream_t st, bool programmatic) {
   if (P.bs == 0 || P.max_q == 0) return cudaSuccess;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(unsigned(P.bs) * unsigned(P.max_q), unsigned(kChunks));
@@ -110,7 +110,7 @@ cudaError_t launch_combine(const Params& P, cudaStream_t st) {
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = programmatic ? 1 : 0;
   return cudaLaunchKernelEx(&cfg, combine_kernel, P);
 }
 

@@ -109,7 +109,7 @@ cudaError_t launch_partial_simt(const Params& P, cudaStream_t st);
 cudaError_t prepare_partial_simt();
 cudaError_t launch_partial_tc(const Params& P, cudaStream_t st);
 cudaError_t prepare_partial_tc();
-cudaError_t launch_combine(const Params& P, cudaStream_t st);
+cudaError_t launch_combine(const Params& P, cudaStream_t st, bool programmatic);
 
 // Kernel geometry constants shared by plan and launch.
 constexpr int kSimtKeyTile = 32;

@@ -334,6 +334,30 @@ def common_component(wl: Workload, a: float = 1.7, b: float = 2.0, seed: int = 7
     return wl
 
 
+def sub_workload(wl: Workload, reqs) -> Workload:
+    """The requests ``reqs`` of ``wl`` as a batch of their own (same pool; CSR
+    offsets re-based, q / out_cache_loc / mask blocks gathered in order)."""
+    kvp, qop, mip = wl.kv_indptr.tolist(), wl.qo_indptr.tolist(), wl.mask_indptr.tolist()
+    kv_idx, ocl, qs, masks = [], [], [], []
+    for r in reqs:
+        kv_idx.append(wl.kv_indices[kvp[r]:kvp[r + 1]])
+        ocl.append(wl.out_cache_loc[qop[r]:qop[r + 1]])
+        qs.append(wl.q[qop[r]:qop[r + 1]])
+        masks.append(wl.custom_mask[mip[r]:mip[r + 1]])
+    prefix = [wl.prefix_lens[r] for r in reqs]
+    sizes = [wl.tree_sizes[r] for r in reqs]
+    cat = lambda xs, dt: torch.cat(xs) if xs else torch.empty(0, dtype=dt)
+    q = torch.cat(qs) if qs else torch.empty((0, NUM_HEADS, D_QK), dtype=torch.bfloat16)
+    return Workload(name=f"{wl.name}_part{len(reqs)}", bs=len(reqs), prefix_lens=prefix, tree_sizes=sizes,
+                    parents=[wl.parents[r] for r in reqs], q=q, kv_pool=wl.kv_pool,
+                    kv_indices=cat(kv_idx, torch.int64), kv_indptr=torch.tensor([0] + list(_cumsum(prefix)), dtype=torch.int32),
+                    out_cache_loc=cat(ocl, torch.int64),
+                    qo_indptr=torch.tensor([0] + list(_cumsum(sizes)), dtype=torch.int64),
+                    custom_mask=cat(masks, torch.uint8),
+                    mask_indptr=torch.tensor([0] + list(_cumsum([m.numel() for m in masks])), dtype=torch.int64),
+                    mask_layout=wl.mask_layout, scale=wl.scale, meta=dict(wl.meta, parent=wl.name, reqs=list(reqs)))
+
+
 def custom(prefix_lens, parents, num_slots, seed, contiguous=False,
            mask_layout=MASK_FULL_ROW, name="custom") -> Workload:
     """Any shape: used by the tests for ragged and degenerate cases."""
@@ -349,6 +373,10 @@ WORKLOADS = {
     "long_random": lambda: long_context(False),
     "mixed": lambda: mixed(),
     "stress": lambda: stress(0),
+    # the stress request shape at 1/8 of the batch on a 300,000-slot pool: a
+    # case small enough (~0.4 GB on the device) for full profiler captures of
+    # the same kernel; per-request traffic scales to the full batch
+    "stress_bs2": lambda: stress(0, pool=randn_bf16((300_000, D_QK), torch.Generator().manual_seed(1015)), bs=2),
     # not one of the five configurations: requests that share one prefix
     "shared_decode": lambda: shared_prefix(16, 32768, 1),
     "shared_tree3": lambda: shared_prefix(16, 32768, 3),

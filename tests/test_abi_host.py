@@ -121,6 +121,10 @@ def test_run_host_checks(lib):
     v = ctypes.c_uint32()
     assert lib.mla_tree_verify_read_device_error(None, ctypes.byref(v), None) == -1
     assert lib.mla_tree_verify_read_static_device_error(None, None) == -1
+    # run_steps: an empty or unknown step mask is a bad argument (checked before anything else runs)
+    P.magic = binding.PLAN_MAGIC
+    for steps in (0, 4, -1):
+        assert lib.mla_tree_verify_run_steps(ctypes.byref(P), *args, fake, 1 << 20, steps, None) == -3
     # the static entry rejects a foreign plan before touching a device
     P.magic = 0
     assert lib.mla_tree_verify_run_static(ctypes.byref(P), *args, None) == -6

@@ -117,9 +117,12 @@ def test_stress_capture_100_replays():
         l = lse.cpu().reshape(-1).numpy()
         if k in (0, 99):
             rows = G.sample_rows(wl, 192, seed=k, include_all_heads_of=1)
-        else:  # one row per request, random token and head
-            toks = [int(wl.qo_indptr[r]) + int(rng.integers(0, 64)) for r in range(wl.bs)]
-            rows = np.array(sorted(t * H + int(rng.integers(0, H)) for t in toks), dtype=np.int64)
+        else:  # every request: one random head of each of 4 distinct tree tokens (4 mask rows per request)
+            rows = []
+            for r in range(wl.bs):
+                for t in rng.choice(64, size=4, replace=False):
+                    rows.append((int(wl.qo_indptr[r]) + int(t)) * H + int(rng.integers(0, H)))
+            rows = np.array(sorted(rows), dtype=np.int64)
         G.compare(wl, o, l, rows=rows, tag=f"stress replay {k}")
         assert np.all(np.isfinite(l)) and np.all(np.isfinite(o))
     assert m.device_error() == 0

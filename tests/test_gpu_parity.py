@@ -109,6 +109,35 @@ def test_bad_slot_sets_error_and_is_masked(flags):
     G.compare(wl, out, lse, ref=ref, tag="bad slot")
 
 
+@pytest.mark.parametrize("nsplit", [1, 3])
+def test_run_steps_partial_then_combine_equals_run(flags, nsplit):
+    """The two launches of a pass, enqueued separately with an event between
+    them, give the result of one run bit for bit."""
+    g = torch.Generator().manual_seed(71)
+    wl = W.custom([500, 1300, 64], [W.random_parents(n, g) for n in (7, 16, 2)], 4096, seed=72)
+    d = G.to_device(wl)
+    m = binding.MlaTreeVerify(wl.bs, wl.max_q_per_req, wl.total_q, wl.max_prefix, flags=flags, nsplit=nsplit)
+    outs = []
+    for split_steps in (False, True):
+        out = torch.full((wl.total_q, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
+        lse = torch.full((wl.total_q, 64), float("nan"), dtype=torch.float32, device="cuda")
+        args = (m.plan, d["q"], d["kv_pool"], d["kv_indices"], d["kv_indptr"], d["out_cache_loc"], d["qo_indptr"],
+                d["custom_mask"], d["mask_indptr"], wl.scale, out, lse, m.workspace)
+        if split_steps:
+            binding.run(*args, steps=binding.STEP_PARTIAL)
+            ev = torch.cuda.Event()
+            ev.record()
+            binding.run(*args, steps=binding.STEP_COMBINE)
+        else:
+            binding.run(*args)
+        torch.cuda.synchronize()
+        outs.append((out.cpu(), lse.cpu()))
+    assert torch.equal(outs[0][0].view(torch.int16), outs[1][0].view(torch.int16))
+    assert torch.equal(outs[0][1].view(torch.int32), outs[1][1].view(torch.int32))
+    assert m.device_error() == 0
+    G.compare(wl, outs[1][0].float().reshape(-1, 512).numpy(), outs[1][1].reshape(-1).numpy(), tag="run_steps")
+
+
 def _padded(t, extra):
     """Device copy of t followed by `extra` zero elements: a declared length
     shorter than the allocation lets a test present offsets past the declared
@@ -197,9 +226,12 @@ def test_request_beyond_plan_bounds_is_flagged(flags):
 
 # ------------------------------------------------------------ named workloads (sampled)
 
-@pytest.mark.parametrize("name", ["batch4", "long_contig", "long_random", "mixed"])
+@pytest.mark.parametrize("name", ["batch4", "long_contig", "long_random", "mixed", "mixed_s2", "mixed_s3"])
 def test_named_workload_sampled(flags, name):
-    wl = W.WORKLOADS[name]()
+    # Mixed is drawn with three seeds: split-K balance across ragged requests is
+    # that configuration's point, so one draw of the request sizes is not enough
+    wl = {"mixed_s2": lambda: W.mixed(seed=2004), "mixed_s3": lambda: W.mixed(seed=3004)}.get(
+        name, W.WORKLOADS.get(name))()
     out, lse = G.run_gpu(wl, flags)
     rows = G.sample_rows(wl, 96, seed=hash(name) % 1000)
     G.compare(wl, out, lse, rows=rows, tag=name)
