@@ -81,14 +81,14 @@ constexpr int STAGES = MTV_TC_STAGES;  // gather pipeline depth
 #endif
 constexpr int NPROD_WARPS = MTV_TC_GATHER_WARPS;
 #ifndef MTV_TC_SOFTMAX_WARPS
-#define MTV_TC_SOFTMAX_WARPS 8
+#define MTV_TC_SOFTMAX_WARPS 4
 #endif
 constexpr int NSOFT_WARPS = MTV_TC_SOFTMAX_WARPS;  // a multiple of 4: WPQ per TMEM lane quarter
 constexpr int WPQ = NSOFT_WARPS / 4;       // softmax warps sharing one lane quarter (one row)
 constexpr int NCOL = NK / WPQ;             // key columns per softmax warp
 constexpr int OCOLS = 256 / WPQ;           // O columns per softmax warp (rescale, epilogue)
 constexpr int XU = NCOL * 2 / 16;          // 16-byte units of one thread's quantised partial row
-constexpr uint32_t kColMask = NCOL >= 32 ? 0xffffffffu : ((1u << NCOL) - 1u);
+constexpr uint64_t kColMask = NCOL >= 64 ? ~0ull : ((1ull << NCOL) - 1ull);
 constexpr int NTHREADS = 32 * (1 + NPROD_WARPS + NSOFT_WARPS);  // warp 0 MMA, then gather, then softmax
 constexpr int KSTEPS2 = NK / 16;          // 4
 constexpr float kRescaleLog2 = 8.0f;      // move the reference max only past 2^8 growth
@@ -135,7 +135,8 @@ static_assert(B_COUNT * 8 <= 256, "barrier area");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kOffQRope % 1024 == 0, "64B-swizzled operand alignment");
 static_assert(NPROD_WARPS <= 8, "one 64-bit validity word per gather warp, 8 per stage");
-static_assert((NSOFT_WARPS == 8 || NSOFT_WARPS == 16) && NCOL % 8 == 0 && (XU & (XU - 1)) == 0,
+static_assert((NSOFT_WARPS == 4 || NSOFT_WARPS == 8 || NSOFT_WARPS == 16) && NCOL % 8 == 0 &&
+                  (XU & (XU - 1)) == 0,
               "softmax column split");
 static_assert(kXRegion % 16 == 0 && kOffRx % 16 == 0 && kOffTx % 16 == 0, "bulk copy alignment");
 
@@ -654,13 +655,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         }
         if (NPROD_WARPS & 1) vm |= vmask_all[sidx * 8 + NPROD_WARPS - 1];
       }
-      const uint32_t vbits = uint32_t(vm >> (NCOL * h)) & kColMask;
+      const uint64_t vbits = (vm >> (NCOL * h)) & kColMask;
       const int64_t kt = k_begin + int64_t(j) * NK + NCOL * h;  // key of this warp's first column
       if (!(valid && vbits == kColMask && kt + NCOL <= R.p)) {  // not an all-prefix, all-valid tile
 #pragma unroll
         for (int cc = 0; cc < NCOL; ++cc) {
           const int64_t k = kt + cc;
-          bool vis = valid && ((vbits >> cc) & 1u);
+          bool vis = valid && ((vbits >> cc) & 1ull);
           if (vis && k >= R.p) vis = tree_visible(P, R, ti, k - R.p);
           if (!vis) x[cc] = -INFINITY;
         }
@@ -669,16 +670,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
 #pragma unroll
       for (int cc = 0; cc < NCOL; cc += 2) mx[(cc >> 1) & 3] = max3(mx[(cc >> 1) & 3], x[cc], x[cc + 1]);
       float mt = max3(fmaxf(mx[0], mx[1]), mx[2], mx[3]) + xmid;  // -inf stays -inf
-      rowmax[((j & 1) * WPQ + h) * ROWS + rr] = mt;
-      if (tracer) MTV_TR(2, j, 9);
-      if (tracer2) MTV_TR(3, j, 9);
-      // combine the tile max of the WPQ warps of this row (bounded mbarrier meeting)
-      __syncwarp();
-      if (lane == 0) mbar_arrive(qbar);
-      ok = wait_fast(qbar, j & 1, W);
-      if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+      if constexpr (WPQ > 1) {
+        rowmax[((j & 1) * WPQ + h) * ROWS + rr] = mt;
+        if (tracer) MTV_TR(2, j, 9);
+        if (tracer2) MTV_TR(3, j, 9);
+        // combine the tile max of the WPQ warps of this row (bounded mbarrier meeting)
+        __syncwarp();
+        if (lane == 0) mbar_arrive(qbar);
+        ok = wait_fast(qbar, j & 1, W);
+        if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
 #pragma unroll
-      for (int hh = 0; hh < WPQ; ++hh) mt = fmaxf(mt, rowmax[((j & 1) * WPQ + hh) * ROWS + rr]);
+        for (int hh = 0; hh < WPQ; ++hh) mt = fmaxf(mt, rowmax[((j & 1) * WPQ + hh) * ROWS + rr]);
+      }
       if (tracer) MTV_TR(2, j, 3);
       if (tracer2) MTV_TR(3, j, 3);
 
@@ -757,7 +760,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       lsum_s[(WPQ + h) * ROWS + rr] = lr;
       __syncwarp();
       if (lane == 0) mbar_arrive(qbar);
-      bool ok = wait_fast(qbar, T & 1, W);
+      // the loop used one phase of this barrier per tile when WPQ > 1
+      bool ok = wait_fast(qbar, WPQ > 1 ? (T & 1) : 0, W);
       alive = __all_sync(0xffffffffu, ok);
     }
     if (alive) {
@@ -790,30 +794,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         }
       }
       __syncwarp();
-      {
-        constexpr int kUnits = OCOLS / 4;                       // 16-byte units per staged row
-        constexpr int kRowsPerPass = 32 / kUnits;               // rows one warp instruction covers
-        const int half = lane / kUnits;
-        const uint32_t unit = uint32_t(lane % kUnits);
-        const int dcol = int(crank) * 256 + OCOLS * h + int(unit) * 4;
-#pragma unroll 4
-        for (int pr = 0; pr < 32 / kRowsPerPass; ++pr) {
-          const int rl = kRowsPerPass * pr + half;  // row within this warp's 32
-          const int64_t g = int64_t(rb) * ROWS + q * 32 + rl;
-          const float4 val = ld_shared_f4(stg + uint32_t(rl) * (OCOLS * 4u) + ((unit ^ (uint32_t(rl) & 15u)) << 4));
-          if (g < rows_req) {
-            const int64_t orow = R.q_off * kHeads + g;
-            if (P.nsplit == 1) {
-              const __nv_bfloat162 a = __floats2bfloat162_rn(val.x, val.y);
-              const __nv_bfloat162 b = __floats2bfloat162_rn(val.z, val.w);
-              *reinterpret_cast<uint2*>(P.out + orow * kDLat + dcol) =
-                  make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
-            } else {
-              *reinterpret_cast<float4*>(P.part_o + (int64_t(split) * P.total_q_max * kHeads + orow) * kDLat + dcol) =
-                  val;
-            }
+      constexpr int kUnits = OCOLS / 4;  // 16-byte units per staged row
+      auto store_unit = [&](int rl, uint32_t unit) {
+        const int64_t g = int64_t(rb) * ROWS + q * 32 + rl;
+        const float4 val = ld_shared_f4(stg + uint32_t(rl) * (OCOLS * 4u) + ((unit ^ (uint32_t(rl) & 15u)) << 4));
+        if (g < rows_req) {
+          const int64_t orow = R.q_off * kHeads + g;
+          const int dcol = int(crank) * 256 + OCOLS * h + int(unit) * 4;
+          if (P.nsplit == 1) {
+            const __nv_bfloat162 a = __floats2bfloat162_rn(val.x, val.y);
+            const __nv_bfloat162 b = __floats2bfloat162_rn(val.z, val.w);
+            *reinterpret_cast<uint2*>(P.out + orow * kDLat + dcol) =
+                make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+          } else {
+            *reinterpret_cast<float4*>(P.part_o + (int64_t(split) * P.total_q_max * kHeads + orow) * kDLat + dcol) =
+                val;
           }
         }
+      };
+      if constexpr (kUnits <= 32) {
+        constexpr int kRowsPerPass = 32 / kUnits;  // rows one warp instruction covers
+#pragma unroll 4
+        for (int pr = 0; pr < 32 / kRowsPerPass; ++pr)
+          store_unit(kRowsPerPass * pr + lane / kUnits, uint32_t(lane % kUnits));
+      } else {
+#pragma unroll 2
+        for (int rl = 0; rl < 32; ++rl)
+#pragma unroll
+          for (int hf = 0; hf < kUnits / 32; ++hf) store_unit(rl, uint32_t(hf * 32 + lane));
       }
       if (valid && crank == 0 && h == 0) {
         const float lse = tot > 0.f ? (m_ref * c + __log2f(tot)) * kLn2 : -INFINITY;
