@@ -21,21 +21,23 @@
 //   2. GEMM1 on the tensor core: S_c[128 x 64] = Q_c . K_c^T, fp32 in TMEM;
 //      the latent part of Q_c is the A operand in TMEM (16 k-steps), its rope
 //      part an A operand in shared memory (2 k-steps);
-//   3. the softmax warps send their partial S to the peer CTA (each warp
-//      stages its 32 rows in shared memory and issues one bulk copy that
-//      completes bytes on the peer's barrier; double-buffered, one tile
-//      ahead) as 16-bit integers relative to the midpoint of each block of 32
-//      values (one row of one warp), with a power-of-two step per block: the
-//      error of a partial score is at most 2^-15 (1 + 2^-10) of the block's
-//      half-range (max - min)/2, whatever the size of the scores (the distributed-shared-
+//   3. the softmax warps (one per TMEM lane quarter by default, all 64 key
+//      columns of its 32 rows) send their partial S to the peer CTA: each
+//      warp stages its 32 rows in shared memory and issues one bulk copy that
+//      completes bytes on the peer's barrier (double-buffered, one tile
+//      ahead).  The values travel as 16-bit integers relative to the midpoint
+//      of each row's NCOL values, with a power-of-two step per row: the error
+//      of a partial score is at most 2^-15 (1 + 2^-10) of the row's half-range
+//      (max - min)/2, whatever the size of the scores (the distributed-shared-
 //      memory link, ~17 B/cycle per CTA, is what this exchange costs, which
-//      rules out fp32), add the peer's partial to their own exact one, apply the tree mask (prefix always visible, tree columns from
-//      custom_mask), and run the fp32 online softmax (two warps per TMEM
-//      lane quarter, 32 key columns each; "Design Decisions and
-//      Trade-Offs": mask -> -inf, streaming max/sum) with a lazily moved
+//      rules out fp32).  Then the warps add the peer's partial to their own
+//      exact one, apply the tree mask (prefix always visible, tree columns
+//      from custom_mask), and run the fp32 online softmax ("Design Decisions
+//      and Trade-Offs": mask -> -inf, streaming max/sum) with a lazily moved
 //      reference max; P (bf16) goes to one of two TMEM buffers.  Each CTA
-//      normalises its own O half with its own softmax sums, so the two views
-//      of S need not be bit-identical;
+//      normalises its own O half with its own softmax sums (of the weights
+//      rounded to bf16, as GEMM2 uses them), so the two views of S need not
+//      be bit-identical;
 //   4. GEMM2: O_c[128 x 256] += P (TMEM, A operand) . V_c, where V_c is this
 //      CTA's 256 latent dims of the same smem tile read as an MN-major operand.
 // The end of a split writes the normalised partial O halves and the LSE of
