@@ -154,9 +154,18 @@ static_assert(sizeof(Ctl) <= kCtlBytes, "control block");
 #ifdef MTV_TRACE
 constexpr int kTraceTiles = 128, kTraceEvents = 16;
 __device__ long long g_trace[4][kTraceTiles][kTraceEvents];
+__device__ int g_trace_cta = 0;  // linear index (y * gridDim.x + x) of the CTA whose pipeline is traced
+constexpr int kTraceCtas = 1 << 14;
+__device__ long long g_cta_trace[kTraceCtas][4];  // per CTA: start ns, end ns, SM id, tiles
+__device__ __forceinline__ long long global_ns() {
+  long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
 #define MTV_TR(role, tile, ev)                                                                            \
   do {                                                                                                    \
-    if (blockIdx.x == 0 && blockIdx.y == 0 && (tile) < kTraceTiles) g_trace[role][tile][ev] = clock64(); \
+    if (int(blockIdx.y * gridDim.x + blockIdx.x) == g_trace_cta && (tile) < kTraceTiles)              \
+      g_trace[role][tile][ev] = clock64();                                                              \
   } while (0)
 #else
 #define MTV_TR(role, tile, ev) \
@@ -234,6 +243,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
   const int r = pair / P.grid_rows, rb = pair % P.grid_rows;
   const int split = blockIdx.y;
   if (threadIdx.x == 0) MTV_TR(1, kTraceTiles - 1, 0);
+#ifdef MTV_TRACE
+  const int cta_id = int(blockIdx.y * gridDim.x + blockIdx.x);
+  if (threadIdx.x == 0 && cta_id < kTraceCtas) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    g_cta_trace[cta_id][0] = global_ns();
+    g_cta_trace[cta_id][1] = 0;
+    g_cta_trace[cta_id][2] = smid;
+    g_cta_trace[cta_id][3] = -1;
+  }
+#endif
   const Req R = load_req(P, r);
   const int64_t rows_req = R.n * kHeads;
   if (int64_t(rb) * ROWS >= rows_req) return;  // both CTAs of the pair take this exit
@@ -241,6 +261,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
   if (split > 0 && k_begin >= R.keys) return;  // empty split: the combine never reads it
   const int64_t k_end = min(R.keys, k_begin + P.split_keys);
   const int T = int((k_end - k_begin + NK - 1) / NK);
+#ifdef MTV_TRACE
+  if (threadIdx.x == 0 && cta_id < kTraceCtas) g_cta_trace[cta_id][3] = T;
+#endif
   uint64_t* vmask_all = reinterpret_cast<uint64_t*>(gbase + kOffVmask);  // [stage][8]
 
   // Slot of gather lane `lane` of warp `pw` for tile j (raw, checked at use).
@@ -456,6 +479,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     const int rr = q * 32 + lane;                  // row within the pair tile = TMEM lane
     const int64_t grow = int64_t(rb) * ROWS + rr;  // row within the request
     const bool valid = grow < rows_req;
+    // Rows are valid in runs of 64 (one tree token), so a warp's 32 rows are
+    // all valid or all past the request's end (the second half of a row block
+    // of a request with an odd tree size).  Such a warp runs a short loop that
+    // keeps the pipeline's protocol -- it sends its (unused) score region,
+    // waits for the peer's, frees S and writes P = 0 -- and skips the softmax.
+    const bool wvalid = __any_sync(0xffffffffu, valid);
     const int64_t ti = grow / kHeads;              // tree token of this row
     const uint32_t lane_off = uint32_t(q * 32) << 16;
     const int64_t out_row = R.q_off * kHeads + grow;  // (token, head) row of q/out/lse
@@ -596,6 +625,48 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       return true;
     };
 
+    if (!wvalid) {
+      // Rows past the request's end (see wvalid): the same barrier and copy
+      // sequence as the loop below, without the arithmetic.
+      auto idle_send = [&](int jn) -> bool {
+        bool ok = wait_fast(bar(B_S_FULL), jn & 1, W);
+        if (!__all_sync(0xffffffffu, ok)) return false;
+        tc_fence_after();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(bar(B_S_FREE));
+          bulk_copy_to_peer(rx_peer + uint32_t(jn & 1) * kXBytes,
+                            base + kOffTx + uint32_t(jn & 1) * kXBytes + uint32_t(wreg) * kXRegion, kXRegion,
+                            peer_sx_full + 8u * uint32_t(jn & 1));
+        }
+        ++nsent;
+        return true;
+      };
+      if (tracer) mbar_arrive_expect_tx(bar(B_SX_FULL0), kXBytes);  // tile 0
+      narmed = 1;
+      alive = idle_send(0);
+      const uint32_t zero[NCOL / 2] = {};
+      for (int j = 0; alive && j < T; ++j) {
+        if (j + 1 < T) {
+          if (tracer) mbar_arrive_expect_tx(bar(B_SX_FULL0 + ((j + 1) & 1)), kXBytes);
+          narmed = j + 2;
+        }
+        bool ok = wait_fast(bar(B_SX_FULL0 + (j & 1)), (j >> 1) & 1, W);
+        if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+        nwaited = j + 1;
+        if (j + 1 < T && !idle_send(j + 1)) { alive = false; break; }
+        if (j >= 2) {  // P buffer j&1 was last read by GEMM2(j-2)
+          ok = wait_fast(bar(B_O_READY0 + (j & 1)), ((j - 2) >> 1) & 1, W);
+          if (!__all_sync(0xffffffffu, ok)) { alive = false; break; }
+        }
+        tc_fence_after();
+        tmem_st_sync(tmem + lane_off + kTmemP + 32 * (j & 1) + (NCOL / 2) * h, zero);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar(B_P_FULL0 + (j & 1)));
+      }
+    } else {
     if (tracer) mbar_arrive_expect_tx(bar(B_SX_FULL0), kXBytes);  // tile 0
     narmed = 1;
     alive = fetch_and_send(0);
@@ -831,6 +902,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         else P.part_lse[int64_t(split) * P.total_q_max * kHeads + out_row] = lse;
       }
     }
+    }
     // Wind-down bookkeeping (also after an abort): the peer learns how many
     // score tiles this warp sent it; the tracer records the armed phases.
     if (lane == 0) {
@@ -877,6 +949,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
   if (warp == 0) tmem_dealloc(tmem, 512);
   cluster_sync();  // both CTAs have received everything sent to them
   if (threadIdx.x == 0) MTV_TR(2, kTraceTiles - 1, 3);
+#ifdef MTV_TRACE
+  if (threadIdx.x == 0 && cta_id < kTraceCtas) g_cta_trace[cta_id][1] = global_ns();
+#endif
 }
 
 }  // namespace
@@ -923,6 +998,13 @@ cudaError_t launch_partial_tc(const Params& P, cudaStream_t st) {
 extern "C" int mtv_trace_read(void* host, size_t bytes) {
   if (bytes > sizeof(mtv::g_trace)) bytes = sizeof(mtv::g_trace);
   return cudaMemcpyFromSymbol(host, mtv::g_trace, bytes) == cudaSuccess ? 0 : -7;
+}
+extern "C" int mtv_trace_select(int cta) {
+  return cudaMemcpyToSymbol(mtv::g_trace_cta, &cta, sizeof cta) == cudaSuccess ? 0 : -7;
+}
+extern "C" int mtv_trace_cta_read(void* host, size_t bytes) {
+  if (bytes > sizeof(mtv::g_cta_trace)) bytes = sizeof(mtv::g_cta_trace);
+  return cudaMemcpyFromSymbol(host, mtv::g_cta_trace, bytes) == cudaSuccess ? 0 : -7;
 }
 extern "C" int mtv_trace_clear() {
   static long long zeros[4 * mtv::kTraceTiles * mtv::kTraceEvents];

@@ -372,6 +372,8 @@ WORKLOADS = {
     "long_contig": lambda: long_context(True),
     "long_random": lambda: long_context(False),
     "mixed": lambda: mixed(),
+    "mixed_s2": lambda: mixed(seed=2004),
+    "mixed_s3": lambda: mixed(seed=3004),
     "stress": lambda: stress(0),
     # the stress request shape at 1/8 of the batch on a 300,000-slot pool: a
     # case small enough (~0.4 GB on the device) for full profiler captures of
