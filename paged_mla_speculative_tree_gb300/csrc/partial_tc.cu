@@ -85,7 +85,7 @@ constexpr int NPROD_WARPS = MTV_TC_GATHER_WARPS;
 #ifndef MTV_TC_SOFTMAX_WARPS
 #define MTV_TC_SOFTMAX_WARPS 4
 #endif
-constexpr int NSOFT_WARPS = MTV_TC_SOFTMAX_WARPS;  // a multiple of 4: WPQ per TMEM lane quarter
+constexpr int NSOFT_WARPS = MTV_TC_SOFTMAX_WARPS;  // 4 or 8: WPQ per TMEM lane quarter
 constexpr int WPQ = NSOFT_WARPS / 4;       // softmax warps sharing one lane quarter (one row)
 constexpr int NCOL = NK / WPQ;             // key columns per softmax warp
 constexpr int OCOLS = 256 / WPQ;           // O columns per softmax warp (rescale, epilogue)
@@ -137,7 +137,7 @@ static_assert(B_COUNT * 8 <= 256, "barrier area");
 static_assert(kSmemBytes <= 227 * 1024, "shared memory budget");
 static_assert(kOffQRope % 1024 == 0, "64B-swizzled operand alignment");
 static_assert(NPROD_WARPS <= 8, "one 64-bit validity word per gather warp, 8 per stage");
-static_assert((NSOFT_WARPS == 4 || NSOFT_WARPS == 8 || NSOFT_WARPS == 16) && NCOL % 8 == 0 &&
+static_assert((NSOFT_WARPS == 4 || NSOFT_WARPS == 8) && NCOL % 8 == 0 &&
                   (XU & (XU - 1)) == 0,
               "softmax column split");
 static_assert(kXRegion % 16 == 0 && kOffRx % 16 == 0 && kOffTx % 16 == 0, "bulk copy alignment");
@@ -173,6 +173,13 @@ __device__ __forceinline__ long long global_ns() {
   } while (0)
 #endif
 
+// Four normalised O values to global memory: fp32 partials or bf16 output.
+__device__ __forceinline__ void store4(float* dst, float4 v) { *reinterpret_cast<float4*>(dst) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* dst, float4 v) {
+  const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y);
+  const __nv_bfloat162 b = __floats2bfloat162_rn(v.z, v.w);
+  *reinterpret_cast<uint2*>(dst) = make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
+}
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -283,6 +290,25 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     pre0 = raw_slot_of(warp - 1, 0);
     pre1 = raw_slot_of(warp - 1, 1);
   }
+  // Likewise the softmax warps load their rows of Q (this CTA's latent half
+  // and rope part) with every load in flight at once; they store them after
+  // the setup.  Rows past the request's end read as zeros.
+  constexpr int kQChunks = 8 / WPQ;  // 16-column TMEM chunks per warp
+  uint4 qpre[kQChunks][4], qrope[4];
+  if (warp > NPROD_WARPS) {
+    const int h0 = (warp - 1 - NPROD_WARPS) >> 2;
+    const int64_t g0 = int64_t(rb) * ROWS + (warp & 3) * 32 + lane;
+    const bool v0 = g0 < rows_req;
+    const uint4* src = reinterpret_cast<const uint4*>(P.q + (R.q_off * kHeads + (v0 ? g0 : 0)) * kDQK);
+#pragma unroll
+    for (int i = 0; i < kQChunks; ++i)
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        qpre[i][u] = v0 ? __ldg(src + (crank * 256 + 32 * (h0 + WPQ * i)) / 8 + u) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      qrope[u] = (v0 && h0 == 0) ? __ldg(src + (512 + crank * 32) / 8 + u) : make_uint4(0u, 0u, 0u, 0u);
+  }
 
   if (tid == 0) {
     for (int s = 0; s < STAGES; ++s) {
@@ -322,22 +348,30 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     if (lane == 0) {
       const uint32_t id1 = idesc_bf16_f32(128, NK, 0, 0);
       const uint32_t id2 = idesc_bf16_f32(128, 256, 0, 1);
+      // Descriptors differ from a stage's base descriptor only in the start
+      // address field (bits 0..13, address >> 4): shared-memory addresses stay
+      // below 2^18, so adding an offset to the low word never carries out of
+      // the field.  (Fewer instructions per MMA on the issuing thread.)
+      auto desc_add = [](uint64_t d, uint32_t off) -> uint64_t {
+        return (d & 0xFFFFFFFF00000000ull) | uint64_t(uint32_t(d) + (off >> 4));
+      };
+      const uint64_t rope_a0 = smem_desc(base + kOffQRope, 16, 512, kSwizzle64B);
       // GEMM1 of tile j: S = Q . K^T into the single S buffer.
       auto gemm1 = [&](int jj) {
         MTV_TR(0, jj, 1);
         fence_proxy_async_smem();  // cp.async wrote the stage through the generic proxy
         tc_fence_after();
         const uint32_t st = base + kOffStages + uint32_t(jj % STAGES) * kStageBytes;
+        const uint64_t b0 = smem_desc(st, 16, 1024, kSwizzle128B);
+        const uint64_t r0 = smem_desc(st + 4 * kChunkBytes, 16, 512, kSwizzle64B);
 #pragma unroll
         for (int kk = 0; kk < 16; ++kk) {
-          const uint64_t bd = smem_desc(st + (kk >> 2) * kChunkBytes + (kk & 3) * 32, 16, 1024, kSwizzle128B);
+          const uint64_t bd = desc_add(b0, uint32_t((kk >> 2) * kChunkBytes + (kk & 3) * 32));
           mma_ts(tmem + kTmemS, tmem + kTmemQ + kk * 8, bd, id1, kk > 0 ? 1u : 0u);
         }
 #pragma unroll
         for (int kk = 0; kk < 2; ++kk) {
-          const uint64_t ad = smem_desc(base + kOffQRope + kk * 32, 16, 512, kSwizzle64B);
-          const uint64_t bd = smem_desc(st + 4 * kChunkBytes + kk * 32, 16, 512, kSwizzle64B);
-          mma_ss(tmem + kTmemS, ad, bd, id1, 1u);
+          mma_ss(tmem + kTmemS, desc_add(rope_a0, uint32_t(kk * 32)), desc_add(r0, uint32_t(kk * 32)), id1, 1u);
         }
         mma_commit(bar(B_S_FULL));
       };
@@ -347,9 +381,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         tc_fence_after();
         const uint32_t st = base + kOffStages + uint32_t(jj % STAGES) * kStageBytes;
         const uint32_t pa = tmem + kTmemP + 32u * uint32_t(jj & 1);
+        const uint64_t v0 = smem_desc(st, kChunkBytes, 1024, kSwizzle128B);
 #pragma unroll
         for (int kk = 0; kk < KSTEPS2; ++kk) {
-          const uint64_t bd = smem_desc(st + kk * 2048, kChunkBytes, 1024, kSwizzle128B);
+          const uint64_t bd = desc_add(v0, uint32_t(kk * 2048));
           mma_ts(tmem + kTmemO, pa + kk * 8, bd, id2, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(bar(B_O_READY0 + (jj & 1)));
@@ -498,32 +533,24 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
     const float c = P.scale_log2;
     const float thr_raw = kRescaleLog2 / c;
 
-    // Q half: latent dims -> TMEM (A operand, column j packs dims 2j, 2j+1; the
-    // warps of a quarter take 16-column chunks in turn); rope dims -> shared
-    // memory in the 64B-swizzled K-major layout (warp h = 0 writes them).
+    // Q half (loaded into registers before the setup): latent dims -> TMEM
+    // (A operand, column j packs dims 2j, 2j+1; the warps of a quarter take
+    // 16-column chunks in turn); rope dims -> shared memory in the 64B-swizzled
+    // K-major layout (warp h = 0 writes them).
     {
-      const __nv_bfloat16* qrow = P.q + out_row * kDQK;
-#pragma unroll 1
-      for (int c0 = 16 * h; c0 < 128; c0 += 16 * WPQ) {
+#pragma unroll
+      for (int i = 0; i < kQChunks; ++i) {
         uint32_t v[16];
-        if (valid) {
-          const uint4* src = reinterpret_cast<const uint4*>(qrow + crank * 256 + 2 * c0);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const uint4 xq = __ldg(src + u);
-            v[4 * u] = xq.x; v[4 * u + 1] = xq.y; v[4 * u + 2] = xq.z; v[4 * u + 3] = xq.w;
-          }
-        } else {
-#pragma unroll
-          for (int u = 0; u < 16; ++u) v[u] = 0u;
-        }
-        tmem_st16_sync(tmem + lane_off + kTmemQ + c0, v);
-      }
-      if (h == 0) {
-        const uint4* src = reinterpret_cast<const uint4*>(qrow + 512 + crank * 32);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const uint4 xq = valid ? __ldg(src + u) : make_uint4(0u, 0u, 0u, 0u);
+          v[4 * u] = qpre[i][u].x; v[4 * u + 1] = qpre[i][u].y; v[4 * u + 2] = qpre[i][u].z; v[4 * u + 3] = qpre[i][u].w;
+        }
+        tmem_st16_sync(tmem + lane_off + kTmemQ + 16 * (h + WPQ * i), v);
+      }
+      if (h == 0) {
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const uint4 xq = qrope[u];
           st_shared_v4(base + kOffQRope + uint32_t(rr) * 64u + ((uint32_t(u) ^ ((uint32_t(rr) >> 1) & 3u)) << 4),
                        xq.x, xq.y, xq.z, xq.w);
         }
@@ -852,12 +879,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       // KV stage area, free once GEMM2(T-1) (the last tensor-core operation)
       // has completed; 16-byte units are XOR-swizzled by row (conflict-free).
       const uint32_t stg = base + kOffStages + uint32_t(sw) * (32u * OCOLS * 4u);  // 32 rows x OCOLS f32
+      constexpr int kLdCols = OCOLS >= 64 ? 64 : 32;  // columns per TMEM load
 #pragma unroll 1
-      for (int c0 = 0; c0 < OCOLS; c0 += 32) {
-        uint32_t v[32];
-        tmem_ld32_sync(tmem + lane_off + kTmemO + OCOLS * h + c0, v);
+      for (int c0 = 0; c0 < OCOLS; c0 += kLdCols) {
+        uint32_t v[kLdCols];
+        tmem_ld_sync(tmem + lane_off + kTmemO + OCOLS * h + c0, v);
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
+        for (int u = 0; u < kLdCols / 4; ++u) {
           const uint32_t unit = uint32_t(c0 / 4 + u);
           st_shared_v4(stg + uint32_t(lane) * (OCOLS * 4u) + ((unit ^ (uint32_t(lane) & 15u)) << 4),
                        __float_as_uint(__uint_as_float(v[4 * u]) * inv),
@@ -868,33 +896,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       }
       __syncwarp();
       constexpr int kUnits = OCOLS / 4;  // 16-byte units per staged row
-      auto store_unit = [&](int rl, uint32_t unit) {
-        const int64_t g = int64_t(rb) * ROWS + q * 32 + rl;
-        const float4 val = ld_shared_f4(stg + uint32_t(rl) * (OCOLS * 4u) + ((unit ^ (uint32_t(rl) & 15u)) << 4));
-        if (g < rows_req) {
-          const int64_t orow = R.q_off * kHeads + g;
-          const int dcol = int(crank) * 256 + OCOLS * h + int(unit) * 4;
-          if (P.nsplit == 1) {
-            const __nv_bfloat162 a = __floats2bfloat162_rn(val.x, val.y);
-            const __nv_bfloat162 b = __floats2bfloat162_rn(val.z, val.w);
-            *reinterpret_cast<uint2*>(P.out + orow * kDLat + dcol) =
-                make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b));
-          } else {
-            *reinterpret_cast<float4*>(P.part_o + (int64_t(split) * P.total_q_max * kHeads + orow) * kDLat + dcol) =
-                val;
-          }
-        }
-      };
-      if constexpr (kUnits <= 32) {
-        constexpr int kRowsPerPass = 32 / kUnits;  // rows one warp instruction covers
-#pragma unroll 4
-        for (int pr = 0; pr < 32 / kRowsPerPass; ++pr)
-          store_unit(kRowsPerPass * pr + lane / kUnits, uint32_t(lane % kUnits));
-      } else {
-#pragma unroll 2
-        for (int rl = 0; rl < 32; ++rl)
+      static_assert(kUnits % 32 == 0, "whole 512-byte row segments per warp");
+      {
+        // The warp's 32 rows are all valid here (see wvalid): row rl of the
+        // warp is output row out_row - lane + rl.  Lane i stores units i,
+        // i + 32, ... of each row: 512 contiguous bytes (fp32) or 256 (bf16)
+        // per warp instruction.  Rows are unrolled by 8 so that the shared
+        // loads of several rows are in flight before their stores.
+        const int64_t row0 = out_row - lane;
+        const int col = int(crank) * 256 + OCOLS * h + 4 * lane;
+        auto store_rows = [&](auto* dst) {
+#pragma unroll 8
+          for (int rl = 0; rl < 32; ++rl) {
+            const uint32_t src = stg + uint32_t(rl) * (OCOLS * 4u) + ((uint32_t(lane) ^ uint32_t(rl & 15)) << 4);
 #pragma unroll
-          for (int hf = 0; hf < kUnits / 32; ++hf) store_unit(rl, uint32_t(hf * 32 + lane));
+            for (int hf = 0; hf < kUnits / 32; ++hf) {
+              const float4 val = ld_shared_f4(src + hf * 512);
+              store4(dst + rl * kDLat + hf * 128, val);
+            }
+          }
+        };
+        if (P.nsplit == 1) store_rows(P.out + row0 * kDLat + col);
+        else store_rows(P.part_o + (int64_t(split) * P.total_q_max * kHeads + row0) * kDLat + col);
       }
       if (valid && crank == 0 && h == 0) {
         const float lse = tot > 0.f ? (m_ref * c + __log2f(tot)) * kLn2 : -INFINITY;
