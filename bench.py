@@ -270,8 +270,11 @@ def run_ours(args):
         {"out": torch.empty((T, 64, 512), dtype=torch.bfloat16),
          "lse": torch.empty((T, 64), dtype=torch.float32)}, dev)
     flags = binding.FLAG_SIMT_FLOOR if args.simt else 0
+    # the batch's request lengths are known on the host when it is planned:
+    # the split count comes from them (an explicit --nsplit overrides)
     m = binding.MlaTreeVerify(wl.bs, wl.max_q_per_req, T, wl.max_prefix, device=local,
-                              mask_layout=wl.mask_layout, flags=flags, nsplit=args.nsplit)
+                              mask_layout=wl.mask_layout, flags=flags, nsplit=args.nsplit,
+                              lengths=(wl.prefix_lens, wl.tree_sizes))
     stream = torch.cuda.current_stream()
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
@@ -402,6 +405,7 @@ def run_ours(args):
         "config": {"workload": full.name, "bs": full.bs, "prefix": full.prefix_lens, "tree": full.tree_sizes,
                    "num_slots": full.num_slots, "heads": 64, "d_qk": 576, "d_v": 512,
                    "kernel": "simt-floor" if args.simt else "tcgen05", "nsplit": int(m.plan.nsplit),
+                   "nsplit_from": "--nsplit" if args.nsplit else "the batch's request lengths",
                    "split_keys": int(m.plan.split_keys),
                    "parallelism": f"requests partitioned over {ws} GPUs" if ws > 1 else "1 GPU",
                    "requests_per_rank": [len(p_) for p_ in parts],

@@ -131,6 +131,34 @@ int mla_tree_verify_plan(int device, int bs, int max_q_per_req, int64_t total_q_
                          mtv_plan_t* plan_out, uint64_t* ws_bytes_out);
 
 /*
+ * mla_tree_verify_choose_nsplit -- a split count for a batch whose request
+ * lengths are known on the host, to pass as nsplit_override to
+ * mla_tree_verify_plan (with max_prefix / max_q_per_req = the batch's
+ * largest p_r / n_r).  The automatic choice of mla_tree_verify_plan sees only
+ * upper bounds and treats every request as the largest; for a ragged batch
+ * this function instead estimates the partial kernel's work units (one per
+ * 128-row block and split, handed to the SM pairs in grid order; empty ones
+ * cost almost nothing) plus the combine's partial traffic, for every
+ * distinct split length, and returns the smallest count within 2 % of the
+ * best estimate ("The Final Solder Joint" -- "The Three-Edits Sequence": a
+ * fixed split grid whose empty splits exit early).  A batch of identical
+ * requests gets the plan's own choice.  Host only; reads no device.
+ *
+ * num_sms        SM count of the device (>= 2).
+ * bs             requests (>= 0).
+ * prefix_lens    host int64 [bs], p_r >= 0 (may be NULL when bs == 0).
+ * tree_sizes     host int32 [bs], n_r >= 0 (may be NULL when bs == 0).
+ * flags          as for mla_tree_verify_plan (MTV_FLAG_SIMT_FLOOR selects the
+ *                SIMT kernel's rule).
+ * nsplit_out     host, receives a count in [1, 64].
+ *
+ * Returns MTV_OK, MTV_E_NULL_POINTER or MTV_E_BAD_ARGUMENT (num_sms < 2,
+ * a negative size, an unknown flag).
+ */
+int mla_tree_verify_choose_nsplit(int num_sms, int bs, const int64_t* prefix_lens, const int32_t* tree_sizes,
+                                  int flags, int* nsplit_out);
+
+/*
  * mla_tree_verify_run -- enqueue one verify-attention pass on `stream`.
  *
  * q              device, bf16 [total_q, 64, 576] row-major (token, head, dim).

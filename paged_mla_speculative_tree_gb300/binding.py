@@ -54,7 +54,7 @@ class MtvError(RuntimeError):
 
 
 _lib = None
-SYMBOLS = ("mla_tree_verify_plan", "mla_tree_verify_run", "mla_tree_verify_run_steps", "mla_tree_verify_strerror",
+SYMBOLS = ("mla_tree_verify_plan", "mla_tree_verify_choose_nsplit", "mla_tree_verify_run", "mla_tree_verify_run_steps", "mla_tree_verify_strerror",
            "mla_tree_verify_clear_device_error", "mla_tree_verify_read_device_error",
            "mla_tree_verify_run_static", "mla_tree_verify_read_static_device_error", "mla_tree_mask_build", "mla_tree_accept", "mla_kv_defrag",
            "mla_tree_group_prefix")
@@ -77,6 +77,8 @@ def load(path: str | None = None):
     lib.mla_tree_verify_plan.argtypes = [I32, I32, I32, I64, I64, I32, I32, I32, I32, I32, I32,
                                          ctypes.POINTER(MtvPlan), ctypes.POINTER(U64)]
     lib.mla_tree_verify_plan.restype = I32
+    lib.mla_tree_verify_choose_nsplit.argtypes = [I32, I32, P, P, I32, ctypes.POINTER(I32)]
+    lib.mla_tree_verify_choose_nsplit.restype = I32
     lib.mla_tree_verify_run.argtypes = [ctypes.POINTER(MtvPlan), P, P, I64, P, I64, P, P, I64, P, P, I64, P,
                                         ctypes.c_float, P, P, P, U64, P]
     lib.mla_tree_verify_run.restype = I32
@@ -123,6 +125,22 @@ def plan(device: int, bs: int, max_q_per_req: int, total_q_max: int, max_prefix:
     if rc != MTV_OK:
         raise MtvError(rc, "mla_tree_verify_plan")
     return p
+
+
+def choose_nsplit(num_sms: int, prefix_lens, tree_sizes, flags: int = 0) -> int:
+    """Split count for a batch with these request lengths (host lists or
+    arrays), to pass as ``nsplit`` to ``plan``."""
+    import numpy as np
+    pl = np.ascontiguousarray(np.asarray(list(prefix_lens), dtype=np.int64))
+    ts = np.ascontiguousarray(np.asarray(list(tree_sizes), dtype=np.int32))
+    if pl.shape != ts.shape:
+        raise ValueError("prefix_lens and tree_sizes differ in length")
+    out = ctypes.c_int(0)
+    rc = load().mla_tree_verify_choose_nsplit(int(num_sms), int(pl.size), pl.ctypes.data if pl.size else None,
+                                              ts.ctypes.data if ts.size else None, int(flags), ctypes.byref(out))
+    if rc != MTV_OK:
+        raise MtvError(rc, "mla_tree_verify_choose_nsplit")
+    return int(out.value)
 
 
 def _ptr(t, dtype, name, empty=None):
@@ -305,7 +323,13 @@ class MlaTreeVerify:
     ``out``/``lse``; it never synchronises, so it can be captured in a graph."""
 
     def __init__(self, bs, max_q_per_req, total_q_max, max_prefix, device=0,
-                 mask_layout=MASK_FULL_ROW, flags=0, nsplit=0):
+                 mask_layout=MASK_FULL_ROW, flags=0, nsplit=0, lengths=None):
+        """``lengths``: optional (prefix_lens, tree_sizes) of the batch the
+        plan is for; with ``nsplit == 0`` the split count then comes from
+        ``choose_nsplit`` instead of the upper bounds alone."""
+        if nsplit == 0 and lengths is not None:
+            sms = torch.cuda.get_device_properties(device).multi_processor_count
+            nsplit = choose_nsplit(sms, lengths[0], lengths[1], flags)
         self.plan = plan(device, bs, max_q_per_req, total_q_max, max_prefix, mask_layout, flags, nsplit)
         self.device = torch.device("cuda", device)
         self.workspace = torch.empty(max(int(self.plan.ws_bytes), 256), dtype=torch.uint8, device=self.device)

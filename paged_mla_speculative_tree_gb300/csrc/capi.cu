@@ -8,6 +8,9 @@
 #include <string.h>
 
 #include <algorithm>
+#include <functional>
+#include <queue>
+#include <vector>
 
 #include "mtv_internal.cuh"
 
@@ -38,6 +41,57 @@ extern const int kTcRowTile;
 extern const int kTcKeyTile;
 }  // namespace mtv
 
+namespace {
+
+// Estimated partial + combine time (us) of a ragged batch split `ns` ways:
+// the partial kernel's work units (one CTA pair per 128-row block and split,
+// in grid order: split-major, then request, then row block) are handed to
+// the first free SM pair; a unit costs a fixed set-up/epilogue time plus its
+// 64-key tiles, an empty one (past its request's rows or keys) almost
+// nothing.  The constants were fitted to measured split-count sweeps on a
+// GB300 at 2.07 GHz (Long, Batch-4, the Stress request shape and three Mixed
+// draws).  split_keys is derived from max_keys exactly as the plan does.
+// With `bound` > 0 the estimate stops early (returning a value above
+// `bound`) once the work divided evenly over the SM pairs already exceeds it.
+double estimate_ragged_us(int slots, int bs, const int64_t* keys, const int64_t* row_blocks, int64_t max_keys,
+                          int64_t max_row_blocks, int64_t rows_total, int ns, int* ns_used, double bound) {
+  constexpr double kTileUs = 1.24, kUnitUs = 6.0, kEmptyUs = 0.2, kCombineUs = 8.0, kHbmBytesPerUs = 6.0e6;
+  const int64_t split_keys = ceil_div(ceil_div(max_keys, ns), kTcKeyTile) * kTcKeyTile;
+  const int64_t used = std::max<int64_t>(1, ceil_div(max_keys, split_keys));
+  *ns_used = int(used);
+  const double combine =
+      used > 1 ? double(used) * double(rows_total) * kDLat * 4.0 * 2.0 / kHbmBytesPerUs + kCombineUs : 0.0;
+  if (bound > 0.0) {
+    double work = 0.0;
+    for (int r = 0; r < bs; ++r) {
+      const int64_t live = std::max<int64_t>(1, ceil_div(keys[r], split_keys));  // splits holding keys
+      work += double(row_blocks[r]) * (double(live) * kUnitUs + double(ceil_div(std::max<int64_t>(1, keys[r]),
+                                                                                kTcKeyTile)) * kTileUs);
+    }
+    if (work / slots + combine > bound) return work / slots + combine;
+  }
+  std::priority_queue<double, std::vector<double>, std::greater<double>> free_at;
+  for (int i = 0; i < slots; ++i) free_at.push(0.0);
+  double makespan = 0.0;
+  for (int64_t s = 0; s < used; ++s) {
+    for (int r = 0; r < bs; ++r) {
+      const int64_t k0 = s * split_keys;
+      const bool live = s == 0 || k0 < keys[r];  // split 0 always writes a result
+      const int64_t tiles = live ? ceil_div(std::max<int64_t>(1, std::min(split_keys, keys[r] - k0)), kTcKeyTile) : 0;
+      for (int64_t rb = 0; rb < max_row_blocks; ++rb) {
+        const double cost = (live && rb < row_blocks[r]) ? kUnitUs + double(tiles) * kTileUs : kEmptyUs;
+        const double t = free_at.top() + cost;
+        free_at.pop();
+        free_at.push(t);
+        makespan = std::max(makespan, t);
+      }
+    }
+  }
+  return makespan + combine;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* mla_tree_verify_strerror(int code) {
@@ -53,6 +107,68 @@ const char* mla_tree_verify_strerror(int code) {
     case MTV_E_DEVICE: return "device unusable (needs an sm_103 GPU; plan device must be current)";
     default: return "unknown error code";
   }
+}
+
+int mla_tree_verify_choose_nsplit(int num_sms, int bs, const int64_t* prefix_lens, const int32_t* tree_sizes,
+                                  int flags, int* nsplit_out) {
+  if (!nsplit_out) return MTV_E_NULL_POINTER;
+  if (num_sms < 2 || bs < 0) return MTV_E_BAD_ARGUMENT;
+  if (flags & ~(MTV_FLAG_SIMT_FLOOR | MTV_FLAG_TEST_SHORT_WAITS)) return MTV_E_BAD_ARGUMENT;
+  if (bs > 0 && (!prefix_lens || !tree_sizes)) return MTV_E_NULL_POINTER;
+  int64_t max_prefix = 0, max_q = 0, rows_total = 0;
+  bool uniform = true;
+  for (int r = 0; r < bs; ++r) {
+    if (prefix_lens[r] < 0 || tree_sizes[r] < 0) return MTV_E_BAD_ARGUMENT;
+    max_prefix = std::max(max_prefix, prefix_lens[r]);
+    max_q = std::max<int64_t>(max_q, tree_sizes[r]);
+    rows_total += int64_t(tree_sizes[r]) * kHeads;
+    uniform = uniform && prefix_lens[r] == prefix_lens[0] && tree_sizes[r] == tree_sizes[0];
+  }
+  // the plan's key bound (a run may present max_prefix + max_q keys)
+  const int64_t max_keys = std::max<int64_t>(1, max_prefix + max_q);
+  if (bs == 0 || max_q == 0) {
+    *nsplit_out = 1;
+    return MTV_OK;
+  }
+  if (flags & MTV_FLAG_SIMT_FLOOR) {
+    *nsplit_out = choose_nsplit_simt(num_sms, int64_t(bs) * max_q, max_keys);
+    return MTV_OK;
+  }
+  const int64_t max_rb = ceil_div(max_q * kHeads, kTcRowTile);
+  if (uniform) {  // the plan's own choice for a batch of equal requests
+    *nsplit_out = choose_nsplit_tc(num_sms, int64_t(bs) * max_rb, max_keys, int64_t(bs) * max_q * kHeads);
+    return MTV_OK;
+  }
+  std::vector<int64_t> keys(bs), rbs(bs);
+  for (int r = 0; r < bs; ++r) {
+    keys[r] = prefix_lens[r] + tree_sizes[r];
+    rbs[r] = ceil_div(int64_t(tree_sizes[r]) * kHeads, kTcRowTile);
+  }
+  // estimate every distinct split count; keep the smallest within 2 % of the best
+  std::vector<std::pair<int, double>> est;
+  int prev_used = 0;
+  double best_so_far = 0.0;  // estimates above 1.02x the best so far cannot be picked: bound them
+  for (int ns = 1; ns <= 64; ++ns) {
+    int used = 0;
+    const double t = estimate_ragged_us(num_sms / 2, bs, keys.data(), rbs.data(), max_keys, max_rb, rows_total, ns,
+                                        &used, best_so_far * 1.02);
+    best_so_far = best_so_far > 0.0 ? std::min(best_so_far, t) : t;
+    if (used == prev_used) continue;  // same split length as a smaller count
+    prev_used = used;
+    est.emplace_back(used, t);
+    if (int64_t(used) * kTcKeyTile >= max_keys) break;  // one tile per split
+  }
+  double best = 1e300;
+  for (const auto& e : est) best = std::min(best, e.second);
+  int pick = 1;
+  for (const auto& e : est) {
+    if (e.second <= best * 1.02) {
+      pick = e.first;
+      break;
+    }
+  }
+  *nsplit_out = pick;
+  return MTV_OK;
 }
 
 int mla_tree_verify_plan(int device, int bs, int max_q_per_req, int64_t total_q_max,

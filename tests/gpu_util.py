@@ -30,12 +30,15 @@ def to_device(wl, dev="cuda"):
 
 
 def run_gpu(wl, flags=0, nsplit=0, dev_tensors=None, total_q_max=None, max_prefix=None, max_q=None,
-            return_err=False, lengths=None):
+            return_err=False, lengths=None, plan_from_lengths=False):
+    """``lengths``: buffer lengths passed to the run; ``plan_from_lengths``:
+    the split count comes from the batch's request lengths (choose_nsplit)."""
     d = dev_tensors or to_device(wl)
     T = total_q_max or wl.total_q
     m = binding.MlaTreeVerify(wl.bs, max_q or wl.max_q_per_req, T, max_prefix or wl.max_prefix,
                               device=torch.cuda.current_device(), mask_layout=wl.mask_layout,
-                              flags=flags, nsplit=nsplit)
+                              flags=flags, nsplit=nsplit,
+                              lengths=(wl.prefix_lens, wl.tree_sizes) if plan_from_lengths else None)
     out = torch.full((T, 64, 512), float("nan"), dtype=torch.bfloat16, device="cuda")
     lse = torch.full((T, 64), float("nan"), dtype=torch.float32, device="cuda")
     m(d["q"], d["kv_pool"], d["kv_indices"], d["kv_indptr"], d["out_cache_loc"], d["qo_indptr"],

@@ -130,6 +130,56 @@ def test_run_host_checks(lib):
     assert lib.mla_tree_verify_run_static(ctypes.byref(P), *args, None) == -6
 
 
+def _choose(lib, sms, prefix, tree, flags=0):
+    import numpy as np
+    pl = np.asarray(prefix, dtype=np.int64)
+    ts = np.asarray(tree, dtype=np.int32)
+    out = ctypes.c_int(-1)
+    rc = lib.mla_tree_verify_choose_nsplit(sms, len(pl), pl.ctypes.data if len(pl) else None,
+                                           ts.ctypes.data if len(ts) else None, flags, ctypes.byref(out))
+    return rc, out.value
+
+
+def test_choose_nsplit_argument_checks(lib):
+    out = ctypes.c_int()
+    assert lib.mla_tree_verify_choose_nsplit(152, 0, None, None, 0, None) == -1
+    assert lib.mla_tree_verify_choose_nsplit(152, 1, None, None, 0, ctypes.byref(out)) == -1
+    assert lib.mla_tree_verify_choose_nsplit(1, 0, None, None, 0, ctypes.byref(out)) == -3
+    assert lib.mla_tree_verify_choose_nsplit(152, -1, None, None, 0, ctypes.byref(out)) == -3
+    assert _choose(lib, 152, [100], [4], flags=0x10)[0] == -3
+    assert _choose(lib, 152, [-1], [4])[0] == -3
+    assert _choose(lib, 152, [100], [-4])[0] == -3
+    assert _choose(lib, 152, [], []) == (0, 1)            # nothing to split
+    assert _choose(lib, 152, [5000, 7000], [0, 0]) == (0, 1)  # no query rows
+
+
+def test_choose_nsplit_uniform_batches_keep_the_plan_rule(lib):
+    # the counts the plan's automatic rule gives these shapes on 152 SMs (the
+    # measured best of split-count sweeps on a GB300)
+    assert _choose(lib, 152, [32768], [32]) == (0, 9)            # Long
+    assert _choose(lib, 152, [5760] * 4, [16] * 4) == (0, 2)     # Batch-4
+    assert _choose(lib, 152, [131072] * 16, [64] * 16) == (0, 4)  # Stress
+    assert _choose(lib, 152, [131072] * 2, [64] * 2) == (0, 7)   # the Stress request shape, 2 requests
+
+
+def test_choose_nsplit_ragged_batches(lib):
+    from paged_mla_speculative_tree_gb300 import workloads as W
+    got = {}
+    for seed in (1004, 2004, 3004):
+        wl = W.mixed(seed=seed)
+        rc, ns = _choose(lib, 152, wl.prefix_lens, wl.tree_sizes)
+        assert rc == 0 and 1 <= ns <= 64
+        got[seed] = ns
+    # seeds 2004 and 3004 measured fastest at 1 and 4-6 splits (the rule from
+    # upper bounds alone picks 3 and 2)
+    assert got == {1004: 3, 2004: 1, 3004: 4}
+    # a lone long request among short ones is split to spread its keys
+    rc, ns = _choose(lib, 152, [200000] + [2000] * 15, [8] * 16)
+    assert rc == 0 and ns > 1
+    # the SIMT floor keeps its own rule
+    assert _choose(lib, 152, [32768], [32], flags=0x1)[0] == 0
+
+
 def test_tree_ops_host_checks(lib):
     fake = ctypes.c_void_p(0x100000)  # never dereferenced: checks fail first
     # mla_tree_mask_build(parents, qo_indptr, kv_indptr, bs, max_q, layout, mask, cap, mask_indptr, err, stream)
