@@ -142,7 +142,8 @@ int mla_tree_verify_plan(int device, int bs, int max_q_per_req, int64_t total_q_
  * distinct split length, and returns the smallest count within 2 % of the
  * best estimate ("The Final Solder Joint" -- "The Three-Edits Sequence": a
  * fixed split grid whose empty splits exit early).  A batch of identical
- * requests gets the plan's own choice.  Host only; reads no device.
+ * requests, or one of more than 65,536 row blocks in all, gets the plan's
+ * own choice.  Host only; reads no device.
  *
  * num_sms        SM count of the device (>= 2).
  * bs             requests (>= 0).

@@ -135,7 +135,9 @@ int mla_tree_verify_choose_nsplit(int num_sms, int bs, const int64_t* prefix_len
     return MTV_OK;
   }
   const int64_t max_rb = ceil_div(max_q * kHeads, kTcRowTile);
-  if (uniform) {  // the plan's own choice for a batch of equal requests
+  // the plan's own choice for a batch of equal requests, and for batches too
+  // large to simulate cheaply (the estimate walks every work unit)
+  if (uniform || int64_t(bs) * max_rb > (int64_t(1) << 16)) {
     *nsplit_out = choose_nsplit_tc(num_sms, int64_t(bs) * max_rb, max_keys, int64_t(bs) * max_q * kHeads);
     return MTV_OK;
   }
