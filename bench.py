@@ -746,15 +746,27 @@ def load_traffic(workload_name, plan):
     return None
 
 
+def _code_only(text: str) -> str:
+    """C/C++ source without comments and blank lines (string literals in
+    these files hold no comment markers)."""
+    import re
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return "\n".join(line.rstrip() for line in text.splitlines() if line.strip())
+
+
 def kernel_revision():
-    """Hash of the sources the partial kernel is built from (its .cu, the
-    headers it includes, and the ABI header)."""
+    """Hash of the code the partial kernel is built from: its .cu and the
+    headers it includes, comments and blank lines removed, plus the ABI
+    header's #define lines (its constants); edits to comments or to host
+    declarations leave it unchanged."""
     import hashlib
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "paged_mla_speculative_tree_gb300", "csrc")
     for f in ("partial_tc.cu", "tc_ptx.cuh", "mtv_internal.cuh"):
-        h.update(open(os.path.join(csrc, f), "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "mla_tree_verify.h"), "rb").read())
+        h.update(_code_only(open(os.path.join(csrc, f)).read()).encode())
+    hdr = _code_only(open(os.path.join(ROOT, "include", "mla_tree_verify.h")).read())
+    h.update("\n".join(line for line in hdr.splitlines() if line.lstrip().startswith("#define")).encode())
     return h.hexdigest()[:16]
 
 

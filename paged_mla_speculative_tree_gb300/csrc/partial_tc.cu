@@ -57,7 +57,8 @@
 // no tensor-core operation, copy or remote write is in flight past that point.
 //
 // Building with -DMTV_TRACE records clock64() timestamps of the pipeline
-// events of the first CTA into a device buffer (read with mtv_trace_read).
+// events of one CTA (chosen with mtv_trace_select, read with mtv_trace_read)
+// and start/end times, SM and tile count of every CTA (mtv_trace_cta_read).
 #include <math.h>
 
 #include "mtv_internal.cuh"
