@@ -12,7 +12,6 @@ import numpy as np
 import pytest
 import torch
 
-import oracle
 from paged_mla_speculative_tree_gb300 import binding
 from paged_mla_speculative_tree_gb300 import workloads as W
 from tests import gpu_util as G

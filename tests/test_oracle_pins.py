@@ -20,7 +20,6 @@ from __future__ import annotations
 import itertools
 import math
 import os
-import re
 import tempfile
 
 import numpy as np

@@ -3,7 +3,6 @@ closed forms for chain and star trees, the reflexive-transitive closure of the
 parent relation (Warshall), invariants, brute force over all root paths for
 acceptance, a hand-derived worked example (tests/golden/tree_steps_example.json)
 and planted mistakes that each pin must catch."""
-import itertools
 
 import numpy as np
 import pytest
