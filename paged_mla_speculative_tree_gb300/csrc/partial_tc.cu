@@ -391,9 +391,11 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
         mma_commit(bar(B_O_READY0 + (jj & 1)));
         mma_commit(bar(B_KV_EMPTY + jj % STAGES));
       };
-      // Event-driven issue: GEMM1(j1) as soon as its stage has landed and the
-      // softmax has read S(j1-1); GEMM2(j2) as soon as P(j2) is in TMEM.  The
-      // two streams never wait on each other's inputs, so a late stage does
+      // Event-driven issue: GEMM1(j1) as soon as the softmax has read S(j1-1)
+      // and its stage has landed; GEMM2(j2) as soon as P(j2) is in TMEM, and
+      // first when both are ready (it frees a stage and a P buffer, and lets
+      // the softmax rescale O sooner; measured 1-2 % faster than GEMM1 first).
+      // The two streams never wait on each other's inputs, so a late stage does
       // not hold back the GEMM2 that frees an earlier one.  Tensor-core
       // operations of one thread run in issue order, and GEMM2(j) is only
       // issued after GEMM1(j).
@@ -402,16 +404,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NTHREADS, 1) partial
       long long t_prog = clock64();
       while (ok && j2 < T) {
         bool did = false;
-        if (j1 < T && mbar_test_wait(bar(B_KV_FULL + j1 % STAGES), (j1 / STAGES) & 1) &&
-            (j1 == 0 || mbar_test_wait(bar(B_S_FREE), (j1 - 1) & 1))) {
-          MTV_TR(0, j1, 0);
-          gemm1(j1);
-          ++j1;
-          did = true;
-        }
         if (j2 < j1 && mbar_test_wait(bar(B_P_FULL0 + (j2 & 1)), (j2 >> 1) & 1)) {
           gemm2(j2);
           ++j2;
+          did = true;
+        }
+        if (j1 < T && (j1 == 0 || mbar_test_wait(bar(B_S_FREE), (j1 - 1) & 1)) &&
+            mbar_test_wait(bar(B_KV_FULL + j1 % STAGES), (j1 / STAGES) & 1)) {
+          MTV_TR(0, j1, 0);
+          gemm1(j1);
+          ++j1;
           did = true;
         }
         if (did) {
